@@ -1,0 +1,24 @@
+"""Flash-LoRA-Attention for B300 (sm_103a).
+
+Public API (thin wrappers over the C ABI in include/flash_lora_attn.h):
+  lr_cache_build(X, A_t, L=None)            L = X . A_cat for every agent at once
+  flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, rank=...)
+  flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0, rank=...)
+  device_error()                            read and clear the device error word
+
+All compute runs in the library's CUDA kernels; the library must have been
+built (`python -m attention_flash_lora_attn_b300.build_lib`).
+"""
+from .binding import (  # noqa: F401
+    EXPORTED,
+    LIB_PATH,
+    FlaError,
+    device_error,
+    flash_lora_attn_decode,
+    flash_lora_attn_prefill,
+    load_library,
+    lr_cache_build,
+    version,
+)
+
+__version__ = "0.1.0"

@@ -1,0 +1,238 @@
+"""ctypes binding over the C ABI in include/flash_lora_attn.h.
+
+Argument marshalling only: every tensor must already live on the current
+CUDA device; the functions pass data pointers, strides and the current torch
+stream to the library, which enqueues its own kernels.  There is no CPU or
+PyTorch fallback: if libflashlora.so is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libflashlora.so")
+
+FLA_OK = 0
+FLA_F32, FLA_BF16 = 0, 1
+KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
+STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "FLA_ERR_WORKSPACE",
+          4: "FLA_ERR_CUDA", 5: "FLA_ERR_DEVICE_TIMEOUT"}
+
+# Every symbol the header declares (tests check that the library exports them).
+EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
+            "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
+            "fla_last_error_message", "fla_device_error", "fla_version")
+
+
+class FlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class AttnDims(ctypes.Structure):
+    _fields_ = [("n_agents", ctypes.c_int32), ("hq", ctypes.c_int32), ("hkv", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("rank", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("l_row_stride", ctypes.c_int64), ("l_agent_stride", ctypes.c_int64),
+                ("softmax_scale", ctypes.c_float), ("kernel", ctypes.c_int32)]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libflashlora.so (built by build_lib.py); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: build it with "
+                              "`python -m attention_flash_lora_attn_b300.build_lib`")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        dims_p = ctypes.POINTER(AttnDims)
+        lib.lr_cache_build.argtypes = [vp, i64, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+        lib.lr_cache_build.restype = ctypes.c_int
+        lib.flash_lora_attn_decode_workspace_size.argtypes = [dims_p, i32, i64]
+        lib.flash_lora_attn_decode_workspace_size.restype = sz
+        lib.flash_lora_attn_decode.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, i64, vp, vp, sz, vp]
+        lib.flash_lora_attn_decode.restype = ctypes.c_int
+        lib.flash_lora_attn_prefill_workspace_size.argtypes = [dims_p, i32, i64]
+        lib.flash_lora_attn_prefill_workspace_size.restype = sz
+        lib.flash_lora_attn_prefill.argtypes = [dims_p, vp, vp, vp, vp, vp, i64, i32, vp, vp, sz, vp]
+        lib.flash_lora_attn_prefill.restype = ctypes.c_int
+        lib.fla_status_string.argtypes = [ctypes.c_int]
+        lib.fla_status_string.restype = ctypes.c_char_p
+        lib.fla_last_error_message.argtypes = []
+        lib.fla_last_error_message.restype = ctypes.c_char_p
+        lib.fla_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+        lib.fla_device_error.restype = ctypes.c_int
+        lib.fla_version.argtypes = []
+        lib.fla_version.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != FLA_OK:
+        msg = load_library().fla_last_error_message().decode(errors="replace")
+        raise FlaError(status, msg)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return FLA_F32
+    if t.dtype == torch.bfloat16:
+        return FLA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors on the current device")
+
+
+def _dense(t: torch.Tensor, name: str):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+# Zero-initialised workspaces, one per (device, stream): the library leaves
+# the ticket words zero after every call, so a workspace is reused as is.
+_workspaces = {}
+
+
+def _workspace(nbytes: int, device: torch.device, stream_ptr: int) -> torch.Tensor:
+    key = (device.index, stream_ptr)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def make_dims(n_agents, hq, hkv, head_dim, rank, dtype_code, l_row_stride, l_agent_stride,
+              scale=None, kernel="auto") -> AttnDims:
+    return AttnDims(n_agents, hq, hkv, head_dim, rank, dtype_code, l_row_stride, l_agent_stride,
+                    0.0 if scale is None else float(scale), KERNELS[kernel])
+
+
+def lr_cache_build(X: torch.Tensor, A_t: torch.Tensor, L: Optional[torch.Tensor] = None, *,
+                   kernel: str = "auto", stream=None) -> torch.Tensor:
+    """L = X . A_t^T for every agent at once (A_t = stacked [A*r, D] down-projections).
+
+    X [n, D] (rows may be strided), A_t [A*r, D] contiguous, L [n, A*r] (rows
+    may be strided; a column slice of a wider tensor is allowed).
+    """
+    lib = load_library()
+    _need_cuda(X, A_t, L)
+    n, D = X.shape
+    N, D2 = A_t.shape
+    if D2 != D:
+        raise ValueError("A_t must be [n_cols, d_model]")
+    if L is None:
+        L = torch.empty((n, N), dtype=X.dtype, device=X.device)
+    if X.stride(1) != 1 or L.stride(1) != 1:
+        raise ValueError("X and L must have unit column stride")
+    _dense(A_t, "A_t")
+    if not (X.dtype == A_t.dtype == L.dtype):
+        raise TypeError("X, A_t and L must share one dtype")
+    _check(lib.lr_cache_build(X.data_ptr(), X.stride(0), A_t.data_ptr(), L.data_ptr(), L.stride(0), n, D, N,
+                              _dtype_code(X), KERNELS[kernel], _stream_ptr(stream)))
+    return L
+
+
+def flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, *, rank: int,
+                           l_agent_stride: Optional[int] = None, scale: Optional[float] = None,
+                           O: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                           kernel: str = "auto", stream=None) -> torch.Tensor:
+    """Decode attention over a packed ragged base cache (see the header for layouts).
+
+    Q [R, A, Hq, d]; K_base, V_base [N, Hkv, d]; L [N, ldL] (unit column
+    stride); B [A, r, Hkv*d]; offsets int32 [R+1] on the device.  Returns O
+    fp32 [R, A, Hq, d].
+    """
+    lib = load_library()
+    _need_cuda(Q, K_base, V_base, L, B, offsets, O, workspace)
+    for t, nm in ((Q, "Q"), (K_base, "K_base"), (V_base, "V_base"), (B, "B")):
+        _dense(t, nm)
+    if L.stride(1) != 1:
+        raise ValueError("L must have unit column stride")
+    if offsets.dtype != torch.int32 or not offsets.is_contiguous():
+        raise TypeError("offsets must be a contiguous int32 tensor")
+    R, A, hq, d = Q.shape
+    N, hkv, d2 = K_base.shape
+    if d2 != d or V_base.shape != K_base.shape:
+        raise ValueError("K_base/V_base must be [N, Hkv, d] matching Q")
+    if l_agent_stride is None:
+        l_agent_stride = rank
+    dims = make_dims(A, hq, hkv, d, rank, _dtype_code(Q), L.stride(0), l_agent_stride, scale, kernel)
+    if O is None:
+        O = torch.empty((R, A, hq, d), dtype=torch.float32, device=Q.device)
+    sp = _stream_ptr(stream)
+    need = lib.flash_lora_attn_decode_workspace_size(ctypes.byref(dims), R, N)
+    if workspace is None and need > 0:
+        workspace = _workspace(need, Q.device, sp)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.flash_lora_attn_decode(ctypes.byref(dims), Q.data_ptr(), K_base.data_ptr(), V_base.data_ptr(),
+                                      L.data_ptr(), B.data_ptr(), offsets.data_ptr(), R, N, O.data_ptr(),
+                                      ws_ptr, ws_bytes, sp))
+    return O
+
+
+def flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0: int, *, rank: int,
+                            l_agent_stride: Optional[int] = None, scale: Optional[float] = None,
+                            O: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                            kernel: str = "auto", stream=None) -> torch.Tensor:
+    """Causal chunked prefill: Q [A, c, Hq, d]; K_base, V_base [n0+c, Hkv, d]; L [n0+c, ldL]."""
+    lib = load_library()
+    _need_cuda(Q, K_base, V_base, L, B, O, workspace)
+    for t, nm in ((Q, "Q"), (K_base, "K_base"), (V_base, "V_base"), (B, "B")):
+        _dense(t, nm)
+    if L.stride(1) != 1:
+        raise ValueError("L must have unit column stride")
+    A, c, hq, d = Q.shape
+    N, hkv, _ = K_base.shape
+    if N < n0 + c:
+        raise ValueError("K_base must hold n0 + chunk tokens")
+    if l_agent_stride is None:
+        l_agent_stride = rank
+    dims = make_dims(A, hq, hkv, d, rank, _dtype_code(Q), L.stride(0), l_agent_stride, scale, kernel)
+    if O is None:
+        O = torch.empty((A, c, hq, d), dtype=torch.float32, device=Q.device)
+    sp = _stream_ptr(stream)
+    need = lib.flash_lora_attn_prefill_workspace_size(ctypes.byref(dims), c, n0)
+    if workspace is None and need > 0:
+        workspace = _workspace(need, Q.device, sp)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.flash_lora_attn_prefill(ctypes.byref(dims), Q.data_ptr(), K_base.data_ptr(), V_base.data_ptr(),
+                                       L.data_ptr(), B.data_ptr(), n0, c, O.data_ptr(), ws_ptr, ws_bytes, sp))
+    return O
+
+
+def device_error() -> int:
+    """Synchronise, then read and clear the library's device error word (0 = none)."""
+    lib = load_library()
+    code = ctypes.c_uint32(0)
+    _check(lib.fla_device_error(ctypes.byref(code)))
+    return code.value
+
+
+def version() -> str:
+    return load_library().fla_version().decode()

@@ -1,0 +1,238 @@
+// Host side of the C ABI declared in include/flash_lora_attn.h.
+//
+// Validation happens here, before anything is enqueued; each entry point then
+// picks a kernel family (tensor-core or SIMT) and launches on the caller's
+// stream.  The library allocates no memory and keeps no per-call state.
+//
+// Unity build: every kernel family is a header included below, so the whole
+// library is one translation unit with one device error word.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "../../include/flash_lora_attn.h"
+#include "fla_common.cuh"
+#include "simt_kernels.cuh"
+#include "decode_tc.cuh"
+#include "build_tc.cuh"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+fla_status fail(fla_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+fla_status ok() { return FLA_OK; }
+
+fla_status check_launch(const char *what) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return FLA_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t dtype_size(int32_t dt) { return dt == FLA_F32 ? 4 : 2; }
+
+// Checks shared by decode and prefill.  Fills `scale`.
+fla_status check_dims(const fla_attn_dims *d, float *scale) {
+  if (!d) return fail(FLA_ERR_INVALID_ARG, "dims is NULL");
+  if (d->n_agents < 1) return fail(FLA_ERR_INVALID_ARG, "n_agents must be >= 1 (got %d)", d->n_agents);
+  if (d->hq < 1 || d->hkv < 1) return fail(FLA_ERR_INVALID_ARG, "hq and hkv must be >= 1");
+  if (d->hq % d->hkv != 0)
+    return fail(FLA_ERR_INVALID_ARG, "hq (%d) must be a multiple of hkv (%d)", d->hq, d->hkv);
+  if (d->head_dim < 1 || d->head_dim > fla::kSimtMaxD || d->head_dim % 4 != 0)
+    return fail(FLA_ERR_UNSUPPORTED, "head_dim %d: must be a multiple of 4 in [4, 256]", d->head_dim);
+  if (d->rank < 1 || d->rank > fla::kSimtMaxR)
+    return fail(FLA_ERR_UNSUPPORTED, "rank %d: must be in [1, 256]", d->rank);
+  if (d->dtype != FLA_F32 && d->dtype != FLA_BF16)
+    return fail(FLA_ERR_INVALID_ARG, "dtype %d is not FLA_F32 or FLA_BF16", d->dtype);
+  if (d->kernel < FLA_KERNEL_AUTO || d->kernel > FLA_KERNEL_TENSOR)
+    return fail(FLA_ERR_INVALID_ARG, "kernel %d is not a fla_kernel", d->kernel);
+  if (d->l_agent_stride < 0) return fail(FLA_ERR_INVALID_ARG, "l_agent_stride must be >= 0");
+  const int64_t need = (int64_t)(d->n_agents - 1) * d->l_agent_stride + d->rank;
+  if (d->l_row_stride < need)
+    return fail(FLA_ERR_INVALID_ARG, "l_row_stride %lld is smaller than the %lld columns the agents read",
+                (long long)d->l_row_stride, (long long)need);
+  if (d->l_agent_stride != 0 && d->l_agent_stride < d->rank)
+    return fail(FLA_ERR_INVALID_ARG, "l_agent_stride must be 0 (shared LR cache) or >= rank");
+  *scale = d->softmax_scale > 0.f ? d->softmax_scale : 1.0f / std::sqrt((float)d->head_dim);
+  return FLA_OK;
+}
+
+template <typename T>
+void launch_simt_attn(const fla::SimtAttnParams &p, int64_t rows, cudaStream_t s) {
+  fla::simt_attn_kernel<T><<<(unsigned)rows, fla::kSimtWarps * 32, 0, s>>>(p);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fla_version(void) { return "0.1.0"; }
+
+const char *fla_status_string(fla_status s) {
+  switch (s) {
+    case FLA_OK: return "FLA_OK";
+    case FLA_ERR_INVALID_ARG: return "FLA_ERR_INVALID_ARG";
+    case FLA_ERR_UNSUPPORTED: return "FLA_ERR_UNSUPPORTED";
+    case FLA_ERR_WORKSPACE: return "FLA_ERR_WORKSPACE";
+    case FLA_ERR_CUDA: return "FLA_ERR_CUDA";
+    case FLA_ERR_DEVICE_TIMEOUT: return "FLA_ERR_DEVICE_TIMEOUT";
+  }
+  return "FLA_ERR_UNKNOWN";
+}
+
+const char *fla_last_error_message(void) { return g_last_error.c_str(); }
+
+fla_status fla_device_error(uint32_t *code) {
+  if (!code) return fail(FLA_ERR_INVALID_ARG, "code is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "cudaDeviceSynchronize: %s", cudaGetErrorString(e));
+  uint32_t v = 0, zero = 0;
+  e = cudaMemcpyFromSymbol(&v, fla::g_device_error, sizeof(v));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(fla::g_device_error, &zero, sizeof(zero));
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "reading the device error word: %s", cudaGetErrorString(e));
+  *code = v;
+  return FLA_OK;
+}
+
+// ---------------------------------------------------------------------------
+fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, int64_t ldl,
+                          int64_t n_tokens, int32_t d_model, int32_t n_cols, int32_t dtype,
+                          int32_t kernel, fla_stream_t stream) {
+  g_last_error.clear();
+  if (n_tokens < 0 || d_model < 1 || n_cols < 1)
+    return fail(FLA_ERR_INVALID_ARG, "n_tokens must be >= 0, d_model and n_cols >= 1");
+  if (dtype != FLA_F32 && dtype != FLA_BF16) return fail(FLA_ERR_INVALID_ARG, "bad dtype %d", dtype);
+  if (kernel < FLA_KERNEL_AUTO || kernel > FLA_KERNEL_TENSOR)
+    return fail(FLA_ERR_INVALID_ARG, "kernel %d is not a fla_kernel", kernel);
+  if (ldx < d_model) return fail(FLA_ERR_INVALID_ARG, "ldx (%lld) < d_model (%d)", (long long)ldx, d_model);
+  if (ldl < n_cols) return fail(FLA_ERR_INVALID_ARG, "ldl (%lld) < n_cols (%d)", (long long)ldl, n_cols);
+  if (n_tokens == 0) return ok();
+  if (!X || !A_t || !L) return fail(FLA_ERR_INVALID_ARG, "X, A_t and L must be non-NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const bool tc_ok = fla::build_tc_supported(X, ldx, A_t, L, ldl, d_model, n_cols, dtype);
+  if (kernel == FLA_KERNEL_TENSOR && !tc_ok)
+    return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build: shape/alignment outside the tensor-core kernel "
+                "(needs bf16, d_model %% 64 == 0, n_cols %% 16 == 0, n_cols <= 512, 16-byte alignment)");
+  if (tc_ok && kernel != FLA_KERNEL_SIMT) {
+    fla_status st = fla::build_tc_launch(X, ldx, A_t, L, ldl, n_tokens, d_model, n_cols, s);
+    if (st != FLA_OK) return fail(st, "lr_cache_build (tensor): %s", fla::build_tc_last_error());
+    return check_launch("lr_cache_build (tensor)");
+  }
+  fla::SimtBuildParams p{X, A_t, L, ldx, ldl, n_tokens, d_model, n_cols};
+  dim3 grid((unsigned)((n_tokens + 63) / 64), (unsigned)((n_cols + 63) / 64));
+  if (grid.x > 0x7fffffffu) return fail(FLA_ERR_UNSUPPORTED, "n_tokens too large");
+  if (dtype == FLA_F32)
+    fla::simt_build_kernel<float><<<grid, 256, 0, s>>>(p);
+  else
+    fla::simt_build_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  return check_launch("lr_cache_build (simt)");
+}
+
+// ---------------------------------------------------------------------------
+size_t flash_lora_attn_decode_workspace_size(const fla_attn_dims *dims, int32_t n_req,
+                                             int64_t total_tokens) {
+  float scale;
+  if (check_dims(dims, &scale) != FLA_OK || n_req < 0 || total_tokens < 0) return 0;
+  if (dims->kernel == FLA_KERNEL_SIMT) return 0;
+  if (!fla::decode_tc_shape_supported(*dims)) return 0;
+  return fla::decode_tc_workspace_bytes(*dims, n_req, total_tokens);
+}
+
+fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, const void *K_base,
+                                  const void *V_base, const void *L, const void *B,
+                                  const int32_t *offsets, int32_t n_req, int64_t total_tokens,
+                                  float *O, void *workspace, size_t workspace_bytes,
+                                  fla_stream_t stream) {
+  g_last_error.clear();
+  float scale;
+  fla_status st = check_dims(dims, &scale);
+  if (st != FLA_OK) return st;
+  if (n_req < 0 || total_tokens < 0) return fail(FLA_ERR_INVALID_ARG, "n_req and total_tokens must be >= 0");
+  if (n_req == 0) return ok();
+  if (!Q || !B || !offsets || !O) return fail(FLA_ERR_INVALID_ARG, "Q, B, offsets and O must be non-NULL");
+  if (total_tokens > 0 && (!K_base || !V_base || !L))
+    return fail(FLA_ERR_INVALID_ARG, "K_base, V_base and L must be non-NULL when total_tokens > 0");
+  if (total_tokens > INT32_MAX) return fail(FLA_ERR_UNSUPPORTED, "total_tokens must fit in int32 (offsets are int32)");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+  const bool shape_tc = fla::decode_tc_shape_supported(*dims);
+  const bool align_tc = aligned16(Q) && aligned16(K_base) && aligned16(V_base) && aligned16(L) &&
+                        aligned16(B) && aligned16(O) && (dims->l_row_stride % 8 == 0);
+  if (dims->kernel == FLA_KERNEL_TENSOR && !(shape_tc && align_tc))
+    return fail(FLA_ERR_UNSUPPORTED, "decode: shape/alignment outside the tensor-core kernel (%s)",
+                fla::decode_tc_limits());
+  if (shape_tc && align_tc && dims->kernel != FLA_KERNEL_SIMT && total_tokens > 0) {
+    const size_t need = fla::decode_tc_workspace_bytes(*dims, n_req, total_tokens);
+    if (need > 0 && (!workspace || workspace_bytes < need))
+      return fail(FLA_ERR_WORKSPACE, "decode: workspace of %zu bytes required, %zu given", need,
+                  workspace ? workspace_bytes : (size_t)0);
+    if (need > 0 && (reinterpret_cast<uintptr_t>(workspace) & 255u))
+      return fail(FLA_ERR_INVALID_ARG, "decode: workspace must be 256-byte aligned");
+    st = fla::decode_tc_launch(*dims, scale, Q, K_base, V_base, L, B, offsets, n_req, total_tokens, O,
+                               workspace, s);
+    if (st != FLA_OK) return fail(st, "decode (tensor): %s", fla::decode_tc_last_error());
+    return check_launch("decode (tensor)");
+  }
+
+  fla::SimtAttnParams p{};
+  p.Q = Q; p.K = K_base; p.V = V_base; p.L = L; p.B = B; p.O = O; p.offsets = offsets;
+  p.l_row_stride = dims->l_row_stride; p.l_agent_stride = dims->l_agent_stride;
+  p.n_agents = dims->n_agents; p.hq = dims->hq; p.hkv = dims->hkv; p.d = dims->head_dim;
+  p.r = dims->rank; p.n_req = n_req; p.prefill = 0; p.scale = scale;
+  const int64_t rows = (int64_t)n_req * dims->n_agents * dims->hq;
+  if (rows > 0x7fffffffLL) return fail(FLA_ERR_UNSUPPORTED, "too many query rows");
+  if (dims->dtype == FLA_F32) launch_simt_attn<float>(p, rows, s);
+  else launch_simt_attn<__nv_bfloat16>(p, rows, s);
+  return check_launch("decode (simt)");
+}
+
+// ---------------------------------------------------------------------------
+size_t flash_lora_attn_prefill_workspace_size(const fla_attn_dims *dims, int32_t chunk, int64_t n0) {
+  (void)dims; (void)chunk; (void)n0;
+  return 0;
+}
+
+fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, const void *K_base,
+                                   const void *V_base, const void *L, const void *B, int64_t n0,
+                                   int32_t chunk, float *O, void *workspace, size_t workspace_bytes,
+                                   fla_stream_t stream) {
+  (void)workspace; (void)workspace_bytes;
+  g_last_error.clear();
+  float scale;
+  fla_status st = check_dims(dims, &scale);
+  if (st != FLA_OK) return st;
+  if (n0 < 0 || chunk < 0) return fail(FLA_ERR_INVALID_ARG, "n0 and chunk must be >= 0");
+  if (chunk == 0) return ok();
+  if (!Q || !K_base || !V_base || !L || !B || !O)
+    return fail(FLA_ERR_INVALID_ARG, "Q, K_base, V_base, L, B and O must be non-NULL");
+  if (dims->kernel == FLA_KERNEL_TENSOR)
+    return fail(FLA_ERR_UNSUPPORTED, "prefill: no tensor-core kernel for this shape yet");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  fla::SimtAttnParams p{};
+  p.Q = Q; p.K = K_base; p.V = V_base; p.L = L; p.B = B; p.O = O; p.offsets = nullptr;
+  p.l_row_stride = dims->l_row_stride; p.l_agent_stride = dims->l_agent_stride; p.n0 = n0;
+  p.n_agents = dims->n_agents; p.hq = dims->hq; p.hkv = dims->hkv; p.d = dims->head_dim;
+  p.r = dims->rank; p.chunk = chunk; p.prefill = 1; p.scale = scale;
+  const int64_t rows = (int64_t)dims->n_agents * chunk * dims->hq;
+  if (rows > 0x7fffffffLL) return fail(FLA_ERR_UNSUPPORTED, "too many query rows");
+  if (dims->dtype == FLA_F32) launch_simt_attn<float>(p, rows, s);
+  else launch_simt_attn<__nv_bfloat16>(p, rows, s);
+  return check_launch("prefill (simt)");
+}
+
+}  // extern "C"

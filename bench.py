@@ -1,0 +1,601 @@
+"""Benchmark: Flash-LoRA-Attention decode queries/s and achieved HBM bandwidth on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--legs all|none]
+
+Headline workload (one GPU): the Llama-3-8B-shaped single-layer decode -
+3 agents, 32 query / 8 kv heads, head_dim 128, r 16, shared context 16384
+tokens, one query token per agent, bf16 storage, fp32 accumulation.
+One step = one flash_lora_attn_decode call (scores, online softmax, P.V_base,
+P.L_i, split merge and the B_i epilogue: one kernel).
+
+Timing: W warm-up steps, then K steps replayed from a CUDA graph between a
+barrier + synchronize on both sides, timed with CUDA events on the launching
+stream.  The step inputs rotate over enough copies of the cache (> 4x the
+126 MB L2) that no step finds its K/V/L tiles in L2.  `e2e` re-times K steps
+through the public Python API with pinned host buffers: each step copies the
+queries host->device, decodes, and reads O back device->host.
+
+Under torchrun each rank runs its own independent copy of the workload
+(weak scaling, no collective on the data path); value = all ranks' queries
+divided by the slowest rank's time.
+
+`--impl reference` times the CPU oracle (fp64, numpy) on this host on a
+bounded sample of the same workload; it is a baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LoRA-attn decode queries/s + achieved HBM GB/s (fraction of B300 peak)"
+HEADLINE = "llama8b_decode"
+L2_BYTES = 126 * 1024 * 1024
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return dict(hbm_gbs=float(pk["hbm_gbs"]), bf16_tflops=float(pk["bf16_tflops"]),
+                    bf16_tflops_sustained=float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                    source="measured")
+    except (OSError, KeyError, ValueError):
+        return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    """Hash of the CUDA sources; a stored ncu traffic figure is used only while it matches."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_flash_lora_attn_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(workload)
+        if e and e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower() in ("active", "1"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, world_size: int, device=None) -> float:
+    if world_size == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world_size: int):
+    if world_size > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- workload bytes / flops
+
+def decode_algorithmic_bytes(w) -> int:
+    """K_base + V_base + every agent's L + B + Q + O for one decode call (the expanded L_i.B_i is not counted)."""
+    N = w.total_tokens
+    kv = 2 * N * w.hkv * w.head_dim * 2
+    lr = N * w.n_agents * w.rank * 2
+    b = w.n_agents * w.rank * w.hkv * w.head_dim * 2
+    q = w.n_req * w.n_agents * w.hq * w.head_dim * 2
+    o = w.n_req * w.n_agents * w.hq * w.head_dim * 4
+    return kv + lr + b + q + o
+
+
+def decode_algorithmic_flops(w) -> int:
+    A, hq, d, r = w.n_agents, w.hq, w.head_dim, w.rank
+    return A * hq * w.total_tokens * (4 * d + 2 * r) + w.n_req * A * hq * 2 * r * d
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def build_decode_copies(w, n_copies, device, seed=0):
+    """n_copies independent seeded decode inputs on the device (drawn there: fast, large)."""
+    import torch
+
+    g = torch.Generator(device=device).manual_seed(seed)
+    A, hq, hkv, d, r, N = w.n_agents, w.hq, w.hkv, w.head_dim, w.rank, w.total_tokens
+    copies = []
+    for _ in range(n_copies):
+        c = dict(
+            Q=torch.randn((w.n_req, A, hq, d), generator=g, device=device).to(torch.bfloat16),
+            K_base=torch.randn((N, hkv, d), generator=g, device=device).to(torch.bfloat16),
+            V_base=torch.randn((N, hkv, d), generator=g, device=device).to(torch.bfloat16),
+            L=torch.randn((N, A * r), generator=g, device=device).to(torch.bfloat16),
+            B=(0.02 * torch.randn((A, r, hkv * d), generator=g, device=device)).to(torch.bfloat16),
+        )
+        import numpy as np
+
+        c["offsets"] = torch.tensor([0] + list(np.cumsum(w.lengths)), dtype=torch.int32, device=device)
+        c["O"] = torch.empty((w.n_req, A, hq, d), dtype=torch.float32, device=device)
+        copies.append(c)
+    return copies
+
+
+def time_graph(fn_list, steps, warmup, stream):
+    """Capture `steps` calls (cycling fn_list) into one CUDA graph; return seconds per step."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            fn_list[i % len(fn_list)]()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            fn_list[i % len(fn_list)]()
+    # one untimed replay (warm the graph), then the timed one
+    with torch.cuda.stream(stream):
+        graph.replay()
+    stream.synchronize()
+    return graph
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+
+    import attention_flash_lora_attn_b300 as fla
+    from attention_flash_lora_attn_b300 import build_lib
+    from workloads import WORKLOADS
+
+    build_lib.build()
+    fla.load_library()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = WORKLOADS[HEADLINE]
+    per_copy = decode_algorithmic_bytes(w)
+    n_copies = max(4, -(-4 * L2_BYTES // per_copy))  # rotating set > 4x L2
+    copies = build_decode_copies(w, n_copies, device, seed=1000 + rank)
+    stream = torch.cuda.Stream(device)
+    workspace = torch.zeros(
+        fla.load_library().flash_lora_attn_decode_workspace_size(
+            __import__("ctypes").byref(fla.binding.make_dims(w.n_agents, w.hq, w.hkv, w.head_dim, w.rank, 1,
+                                                             w.n_agents * w.rank, w.rank)),
+            w.n_req, w.total_tokens) + 256, dtype=torch.uint8, device=device)
+
+    def make_call(c):
+        def call():
+            fla.flash_lora_attn_decode(c["Q"], c["K_base"], c["V_base"], c["L"], c["B"], c["offsets"],
+                                       rank=w.rank, O=c["O"], workspace=workspace, kernel="tensor")
+        return call
+
+    calls = [make_call(c) for c in copies]
+    graph = time_graph(calls, args.steps, args.warmup, stream)
+
+    # ---- timed region: K steps from the graph, events on the launching stream
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk, torch.cuda.stream(stream):
+        # replay() launches on the current stream, which is `stream` here
+        start.record(stream)
+        graph.replay()
+        end.record(stream)
+        torch.cuda.synchronize()
+    barrier(ws)
+    t_local = start.elapsed_time(end) / 1e3
+    t = max_over_ranks(t_local, ws, device)
+    queries_per_step = w.n_req * w.n_agents
+    value = ws * queries_per_step * args.steps / t
+    ms_per_step = t / args.steps * 1e3
+    assert fla.device_error() == 0
+
+    # ---- e2e: public API, pinned host Q in, O out, every step
+    Qh = [c["Q"].cpu().pin_memory() for c in copies]
+    Oh = torch.empty(copies[0]["O"].shape, dtype=torch.float32).pin_memory()
+    Qd = torch.empty_like(copies[0]["Q"])
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            c = copies[i % n_copies]
+            Qd.copy_(Qh[i % n_copies], non_blocking=True)
+            fla.flash_lora_attn_decode(Qd, c["K_base"], c["V_base"], c["L"], c["B"], c["offsets"], rank=w.rank,
+                                       O=c["O"], workspace=workspace)
+            Oh.copy_(c["O"], non_blocking=True)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            c = copies[i % n_copies]
+            Qd.copy_(Qh[i % n_copies], non_blocking=True)
+            fla.flash_lora_attn_decode(Qd, c["K_base"], c["V_base"], c["L"], c["B"], c["offsets"], rank=w.rank,
+                                       O=c["O"], workspace=workspace)
+            Oh.copy_(c["O"], non_blocking=True)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, device)
+    e2e_value = ws * queries_per_step * args.steps / t_e2e
+
+    peaks = load_peaks()
+    step_s = t_local / args.steps
+    achieved_gbs = per_copy / step_s / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) Q/K/V/L, B ~ N(0, 0.02^2)); no dataset or trained weights",
+        "config": {
+            "workload": "Llama-3-8B-shaped single-layer decode: 3 agents, 32 q / 8 kv heads, head_dim 128, "
+                        "r 16, shared context 16384 tokens, 1 query token per agent",
+            "n_agents": w.n_agents, "hq": w.hq, "hkv": w.hkv, "head_dim": w.head_dim, "rank": w.rank,
+            "context_tokens": w.total_tokens, "queries_per_step": queries_per_step,
+            "parallelism": f"replicas x{ws} (independent workloads, no collective)",
+            "l2": f"inputs rotate over {n_copies} copies ({n_copies * per_copy / 1e6:.0f} MB > 4x the 126 MB L2)",
+            "timing": "CUDA graph of K decode launches, CUDA events on the launching stream",
+        },
+        "roofline": {
+            "bound": "hbm",
+            "achieved": achieved_gbs,
+            "peak": peaks["hbm_gbs"],
+            "unit": "GB/s",
+            "frac": achieved_gbs / peaks["hbm_gbs"],
+            "traffic": stored_traffic(HEADLINE),
+            "kernel": "decode_tc_kernel",
+            "algorithmic_bytes_per_launch": per_copy,
+            "peak_source": peaks["source"],
+            "frac_of_nominal_8tbs": achieved_gbs / 8000.0,
+        },
+        "e2e": {"value": e2e_value, "unit": "queries/s",
+                "h2d_bytes_per_step": int(copies[0]["Q"].numel() * 2),
+                "d2h_bytes_per_step": int(copies[0]["O"].numel() * 4)},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+    }
+    del copies, calls, graph
+    torch.cuda.empty_cache()
+    if rank == 0 and args.legs == "all":
+        line["legs"] = run_legs(args, device, peaks)
+    if rank == 0 and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(w)
+    return line
+
+
+def _median_launch_s(fn, reps, stream, flush=None):
+    """Median device time of fn() over reps launches (events on `stream`; optional L2 flush between)."""
+    import torch
+
+    times = []
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            fn()
+        for _ in range(reps):
+            if flush is not None:
+                flush()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            times.append(a.elapsed_time(b) / 1e3)
+    return statistics.median(times)
+
+
+def run_legs(args, device, peaks, only=None):
+    """The other hot-path rows, each timed alone: median of event-timed launches.
+
+    `only` (a leg name such as "llama70b_decode/decode") runs that leg alone,
+    which is how the ncu captures select one kernel on one workload.
+
+    Inputs larger than L2 need no flush; the 512-token chunk workloads are
+    preceded by a 256 MB write that evicts L2.
+    """
+    import numpy as np
+    import torch
+
+    import attention_flash_lora_attn_b300 as fla
+    from workloads import WORKLOADS
+
+    reps = max(5, min(args.steps, 20)) if only is None else args.steps
+    stream = torch.cuda.Stream(device)
+
+    def want(name):
+        return only is None or only == name
+    g = torch.Generator(device=device).manual_seed(7)
+    scratch = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=device)
+
+    def flush():
+        scratch.fill_(1.0)
+
+    def rnd(shape, std=1.0):
+        return (std * torch.randn(shape, generator=g, device=device)).to(torch.bfloat16)
+
+    out = {}
+    # ---- LR-cache build of a 512-token chunk (4 agents, r 16) and the causal chunked prefill
+    w = WORKLOADS["llama8b_prefill"]
+    A, r, D, c, n0 = w.n_agents, w.rank, w.d_model, w.chunk, w.n0
+    X, A_t = rnd((c, D)), rnd((A * r, D), D ** -0.5)
+    L = rnd((n0 + c, A * r))
+    if want("llama8b_prefill/lr_cache_build"):
+        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_t, L[n0:]), reps, stream, flush)
+        flops, byts = 2 * c * D * A * r, (c * D + A * r * D + c * A * r) * 2
+        out["llama8b_prefill/lr_cache_build"] = {
+            "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
+            "gbs": byts / t / 1e9, "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
+    if want("llama8b_prefill/prefill"):
+        Q, K, V = rnd((A, c, w.hq, w.head_dim)), rnd((n0 + c, w.hkv, w.head_dim)), rnd((n0 + c, w.hkv, w.head_dim))
+        B = rnd((A, r, w.hkv * w.head_dim), 0.02)
+        O = torch.empty((A, c, w.hq, w.head_dim), dtype=torch.float32, device=device)
+        t = _median_launch_s(lambda: fla.flash_lora_attn_prefill(Q, K, V, L, B, n0, rank=r, O=O),
+                             max(3, reps // 4), stream, flush)
+        # causal: query p sees n0+p+1 keys; QK^T and PV over d, PL over r, (PL)B once per query
+        keys = sum(n0 + p + 1 for p in range(c))
+        flops = A * w.hq * keys * (4 * w.head_dim + 2 * r) + A * c * w.hq * 2 * r * w.head_dim
+        out["llama8b_prefill/prefill"] = {"us": t * 1e6, "tflops": flops / t / 1e12,
+                                          "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"]}
+        del Q, K, V, B, O
+    del X, A_t, L
+    # ---- decode legs (inputs larger than L2)
+    for name in ("llama8b_decode", "llama8b_ragged", "llama70b_decode"):
+        if not want(f"{name}/decode"):
+            continue
+        w = WORKLOADS[name]
+        N, A, r = w.total_tokens, w.n_agents, w.rank
+        Q, K, V = rnd((w.n_req, A, w.hq, w.head_dim)), rnd((N, w.hkv, w.head_dim)), rnd((N, w.hkv, w.head_dim))
+        L, B = rnd((N, A * r)), rnd((A, r, w.hkv * w.head_dim), 0.02)
+        offs = torch.tensor([0] + list(np.cumsum(w.lengths)), dtype=torch.int32, device=device)
+        O = torch.empty((w.n_req, A, w.hq, w.head_dim), dtype=torch.float32, device=device)
+        fits_l2 = decode_algorithmic_bytes(w) < L2_BYTES
+        t = _median_launch_s(lambda: fla.flash_lora_attn_decode(Q, K, V, L, B, offs, rank=r, O=O), reps, stream,
+                             flush if fits_l2 else None)
+        byts = decode_algorithmic_bytes(w)
+        out[f"{name}/decode"] = {"us": t * 1e6, "queries_per_s": w.n_req * A / t, "gbs": byts / t / 1e9,
+                                 "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
+        del Q, K, V, L, B, O
+    # ---- full LR-cache build, 131072 x 8192 . 8192 x 320
+    w = WORKLOADS["llama70b_decode"]
+    if want("llama70b_decode/lr_cache_build"):
+        n, D, Nc = w.build_tokens, w.d_model, w.n_agents * w.rank
+        X, A_t = rnd((n, D)), rnd((Nc, D), D ** -0.5)
+        L = torch.empty((n, Nc), dtype=torch.bfloat16, device=device)
+        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_t, L), max(3, reps // 2), stream)
+        flops, byts = 2 * n * D * Nc, (n * D + Nc * D + n * Nc) * 2
+        out["llama70b_decode/lr_cache_build"] = {
+            "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
+            "gbs": byts / t / 1e9, "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
+        del X, A_t, L
+    del scratch
+    torch.cuda.empty_cache()
+    assert fla.device_error() == 0
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle arm
+
+def oracle_sample_rate(w, budget_s=10.0, max_reps=50):
+    """Oracle queries/s on a bounded sample: one agent's query (all its heads) per repetition."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from workloads import make_decode_inputs
+
+    x = make_decode_inputs(w, seed=0)
+    r = w.rank
+    reps, t_total = 0, 0.0
+    while reps < max_reps and t_total < budget_s:
+        a = reps % w.n_agents
+        t0 = time.perf_counter()
+        oracle.decode(x["Q"][:, a:a + 1], x["K_base"], x["V_base"], x["L"][:, a * r:(a + 1) * r],
+                      x["B"][a:a + 1], x["offsets"].numpy(), rank=r)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    cores = len(os.sched_getaffinity(0))
+    threads = torch.get_num_threads()
+    return reps / t_total, reps, t_total, cores, threads
+
+
+def cpu_baseline(w):
+    rate, reps, secs, cores, threads = oracle_sample_rate(w)
+    return {"value": rate, "unit": "queries/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} single-agent decode queries (all 32 heads, 16384 tokens) of the "
+                      f"headline workload, fp64 numpy, {secs:.1f} s; BLAS threads {threads}"}
+
+
+def run_reference(args):
+    from workloads import WORKLOADS
+
+    w = WORKLOADS[HEADLINE]
+    import numpy as np
+    import torch
+
+    import oracle
+    from workloads import make_decode_inputs
+
+    x = make_decode_inputs(w, seed=0)
+    r = w.rank
+
+    def step(i):
+        a = i % w.n_agents
+        oracle.decode(x["Q"][:, a:a + 1], x["K_base"], x["V_base"], x["L"][:, a * r:(a + 1) * r],
+                      x["B"][a:a + 1], x["offsets"].numpy(), rank=r)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    t = time.perf_counter() - t0
+    value = args.steps / t
+    cores = len(os.sched_getaffinity(0))
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "queries/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": t / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded N(0,1) Q/K/V/L, B ~ N(0, 0.02^2))",
+        "config": {"workload": "Llama-3-8B-shaped single-layer decode: 3 agents, 32 q / 8 kv heads, head_dim "
+                               "128, r 16, shared context 16384 tokens, 1 query token per agent",
+                   "sample": "one agent's decode query (all 32 heads) per step"},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} single-agent decode queries of the headline workload, fp64 "
+                                   f"numpy, BLAS threads {torch.get_num_threads()}"},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+# ----------------------------------------------------------------------------- main
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--legs", choices=["all", "none"], default="all")
+    ap.add_argument("--only", default=None,
+                    help="run one leg alone (e.g. llama70b_decode/decode) and print its numbers")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+
+    if args.only:
+        import torch
+
+        import attention_flash_lora_attn_b300 as fla
+        from attention_flash_lora_attn_b300 import build_lib
+
+        build_lib.build()
+        fla.load_library()
+        device = torch.device("cuda", local)
+        torch.cuda.set_device(device)
+        print(json.dumps({"only": args.only, **run_legs(args, device, load_peaks(), only=args.only)}))
+        return 0
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return 0
+
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    line = run_ours(args, ws, rank, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,192 @@
+/*
+ * flash_lora_attn.h - C ABI of the Flash-LoRA-Attention library (B300, sm_103a).
+ *
+ * The method (LRAgent technical summary, gist.science, "Metodologia"):
+ *   - section 1 "Descomposicion de la Cache": an agent's value cache is a base
+ *     part shared by all agents plus a LoRA adapter part, V_i = V_base + dV_i;
+ *   - section 2, BaseShared: the adapter part is kept in low-rank form, the LR
+ *     cache L_i = X . A_i of width r, expanded by the up-projection B_i only
+ *     when needed; BaseLRShared: A is shared, so one LR cache serves all agents;
+ *   - section 3 "Flash-LoRA-Attention": attention over the decomposed cache is
+ *     evaluated as P.V_base + (P.L_i).B_i instead of P.(V_base + L_i.B_i), so
+ *     L_i.B_i is never expanded to full width and B_i is applied once per query.
+ * PReCache abstract (arxivdaily), PreLRShared: every agent's LR cache is built
+ * when the shared context is first processed (lr_cache_build over all agents).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to caller-owned memory on the
+ *     current CUDA device; the library never allocates, frees or keeps them.
+ *   - Tensors are dense row-major unless a stride argument says otherwise.
+ *   - Calls are enqueued on `stream` (NULL = the legacy default stream), are
+ *     asynchronous and never synchronise the host.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns an error status and launches nothing.
+ *   - Errors never cross the ABI as exceptions.  fla_last_error_message()
+ *     returns a thread-local description of the last failure.
+ *   - Device-side waits are bounded.  A kernel whose wait runs out sets a
+ *     device error word and returns early (its outputs are then undefined);
+ *     read and clear it with fla_device_error() after synchronising.
+ *   - Storage dtype: FLA_BF16 (fp32 accumulation) or FLA_F32.  Attention
+ *     outputs O are always fp32.
+ */
+#ifndef FLASH_LORA_ATTN_H_
+#define FLASH_LORA_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FLA_API __attribute__((visibility("default")))
+#else
+#define FLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; NULL selects the legacy default stream. */
+typedef struct CUstream_st *fla_stream_t;
+
+typedef enum {
+  FLA_OK = 0,
+  FLA_ERR_INVALID_ARG = 1,    /* null pointer, bad size, misaligned pointer, ... */
+  FLA_ERR_UNSUPPORTED = 2,    /* valid but outside what the kernels implement */
+  FLA_ERR_WORKSPACE = 3,      /* workspace missing or smaller than required */
+  FLA_ERR_CUDA = 4,           /* a CUDA runtime/driver call failed (no device, launch error) */
+  FLA_ERR_DEVICE_TIMEOUT = 5  /* reported by fla_device_error(): a bounded wait ran out */
+} fla_status;
+
+typedef enum { FLA_F32 = 0, FLA_BF16 = 1 } fla_dtype;
+
+/* Kernel family.  AUTO picks the tensor-core kernels where the shape allows
+ * and the plain CUDA-core kernels otherwise.  SIMT forces the CUDA-core
+ * kernels (every supported shape); TENSOR fails with FLA_ERR_UNSUPPORTED when
+ * the shape is outside the tensor-core kernels' limits. */
+typedef enum { FLA_KERNEL_AUTO = 0, FLA_KERNEL_SIMT = 1, FLA_KERNEL_TENSOR = 2 } fla_kernel;
+
+/* Shape of the attention problem (decode and prefill). */
+typedef struct {
+  int32_t n_agents;       /* A >= 1: agents sharing the base cache */
+  int32_t hq;             /* query heads per agent, hq % hkv == 0 */
+  int32_t hkv;            /* key/value heads; q head j reads kv head j / (hq/hkv) */
+  int32_t head_dim;       /* d: 64 or 128 (tensor kernels); 1..256, multiple of 4 (SIMT) */
+  int32_t rank;           /* r: LoRA rank, 1..256 */
+  int32_t dtype;          /* fla_dtype of Q, K_base, V_base, L and B */
+  int64_t l_row_stride;   /* elements between consecutive tokens of L */
+  int64_t l_agent_stride; /* elements between agents' column blocks of L: r for
+                             per-agent LR caches (BaseShared), 0 for one LR cache
+                             shared by every agent (BaseLRShared) */
+  float softmax_scale;    /* <= 0 selects 1/sqrt(head_dim) */
+  int32_t kernel;         /* fla_kernel */
+} fla_attn_dims;
+
+/*
+ * lr_cache_build - L[t, c] = sum_k X[t, k] * A_t[c, k]   (L = X . A_cat)
+ *
+ * LRAgent summary, Metodologia section 2 (BaseShared: the LR cache stores the
+ * LoRA down-projection X.A_i at width r); PReCache abstract (PreLRShared:
+ * all agents' LR caches built in one pass over the context).
+ *
+ *   X      [n_tokens, d_model], row stride ldx elements      (input)
+ *   A_t    [n_cols, d_model], dense: row c is column c of A_cat = [A_1|...|A_A],
+ *          i.e. the stacked nn.Linear weights of the agents' down-projections,
+ *          agent-major (agent i owns rows [i*r, (i+1)*r))    (input)
+ *   L      [n_tokens, n_cols] written with row stride ldl elements (output;
+ *          other columns of a wider L are left untouched)
+ *   dtype  storage type of X, A_t and L; fp32 accumulation.
+ *   kernel fla_kernel.  The tensor-core path needs bf16, d_model % 64 == 0,
+ *          n_cols % 16 == 0, n_cols <= 512, 16-byte aligned pointers and
+ *          ldx, ldl multiples of 8.
+ * Errors: FLA_ERR_INVALID_ARG for null pointers with n_tokens > 0, negative
+ * sizes, ldx < d_model or ldl < n_cols.  n_tokens == 0 is a no-op.
+ */
+FLA_API fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, int64_t ldl,
+                          int64_t n_tokens, int32_t d_model, int32_t n_cols, int32_t dtype,
+                          int32_t kernel, fla_stream_t stream);
+
+/*
+ * flash_lora_attn_decode - one query token per agent per request.
+ *
+ * For request q, agent a, query head j (kv head h = j / (hq/hkv)) and the
+ * tokens t of request q (offsets[q] <= t < offsets[q+1]):
+ *   s_t = softmax_scale * <Q[q,a,j,:], K_base[t,h,:]>,  P = softmax_t(s)
+ *   O[q,a,j,:] = sum_t P_t V_base[t,h,:] + (sum_t P_t L[t, a*l_agent_stride + (0..r-1)]) . B[a, :, h*d:(h+1)*d]
+ * i.e. softmax(Q.K_base^T/sqrt(d)).(V_base + L_a.B_a) evaluated in the
+ * reordered form of LRAgent section 3; L_a.B_a is never formed.  Every
+ * agent's query rows for a kv head are served from one read of each K_base /
+ * V_base tile.  A request with no tokens gets O = 0.
+ *
+ *   Q        [n_req, A, hq, d]                              (input)
+ *   K_base   [total_tokens, hkv, d]  requests packed by offsets  (input)
+ *   V_base   [total_tokens, hkv, d]                         (input)
+ *   L        [total_tokens, l_row_stride]                   (input)
+ *   B        [A, r, hkv*d]                                  (input)
+ *   offsets  device int32 [n_req + 1], offsets[0] == 0, non-decreasing,
+ *            offsets[n_req] == total_tokens                 (input)
+ *   O        fp32 [n_req, A, hq, d]                         (output)
+ *   workspace device scratch of at least
+ *            flash_lora_attn_decode_workspace_size() bytes, 256-byte
+ *            aligned.  It must be all-zero before the first call that uses it;
+ *            every call leaves it in that state again, so it can be reused by
+ *            later calls on the same stream (calls that overlap on the GPU
+ *            must use different workspaces).
+ * Errors: INVALID_ARG (null pointer, hq % hkv, offsets layout on the host
+ * side, strides), UNSUPPORTED (shape outside the selected kernel's limits),
+ * WORKSPACE (too small), CUDA (launch failure).
+ */
+FLA_API size_t flash_lora_attn_decode_workspace_size(const fla_attn_dims *dims, int32_t n_req,
+                                             int64_t total_tokens);
+FLA_API fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, const void *K_base,
+                                  const void *V_base, const void *L, const void *B,
+                                  const int32_t *offsets, int32_t n_req, int64_t total_tokens,
+                                  float *O, void *workspace, size_t workspace_bytes,
+                                  fla_stream_t stream);
+
+/*
+ * flash_lora_attn_prefill - causal chunked prefill of `chunk` new tokens for
+ * every agent over a shared context of n0 cached tokens.
+ *
+ * The query at chunk position p (absolute position n0 + p) sees keys
+ * 0 .. n0 + p inclusive:
+ *   O[a,p,j,:] = softmax over t <= n0+p of (scale <Q[a,p,j,:], K_base[t,h,:]>)
+ *                applied to V_base[t,h,:] + L[t, a-block] . B[a, :, h*d:(h+1)*d]
+ * evaluated as P.V_base + (P.L_a).B_a (B applied once per query block).
+ *
+ *   Q        [A, chunk, hq, d]                   (input)
+ *   K_base   [n0 + chunk, hkv, d]                (input; the chunk's keys appended)
+ *   V_base   [n0 + chunk, hkv, d]                (input)
+ *   L        [n0 + chunk, l_row_stride]          (input; the chunk's rows built
+ *                                                 by lr_cache_build beforehand)
+ *   B        [A, r, hkv*d]                       (input)
+ *   O        fp32 [A, chunk, hq, d]              (output)
+ *   workspace as for decode, flash_lora_attn_prefill_workspace_size() bytes
+ *            (may be 0 bytes / NULL when the size query returns 0).
+ * Errors as for decode.
+ */
+FLA_API size_t flash_lora_attn_prefill_workspace_size(const fla_attn_dims *dims, int32_t chunk, int64_t n0);
+FLA_API fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, const void *K_base,
+                                   const void *V_base, const void *L, const void *B, int64_t n0,
+                                   int32_t chunk, float *O, void *workspace,
+                                   size_t workspace_bytes, fla_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+FLA_API const char *fla_status_string(fla_status status);
+
+/* Description of the last failure on the calling thread ("" if none). */
+FLA_API const char *fla_last_error_message(void);
+
+/* Reads, and resets to 0, the device error word of the current device.
+ * Synchronises the device first.  Writes 0 (no error) or a nonzero code that
+ * identifies the bounded wait that ran out; returns FLA_ERR_CUDA if the read
+ * itself fails. */
+FLA_API fla_status fla_device_error(uint32_t *code);
+
+/* Library version, e.g. "0.1.0". */
+FLA_API const char *fla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASH_LORA_ATTN_H_ */

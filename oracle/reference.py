@@ -155,12 +155,14 @@ def decode_reordered(Q, K_base, V_base, L, B, offsets, rank: int, scale: float =
 
 
 def prefill(Q, K_base, V_base, L, B, n0: int, rank: int, scale: float = None,
-            agent_stride: int = None) -> np.ndarray:
+            agent_stride: int = None, positions=None) -> np.ndarray:
     """Causal chunked prefill of c new tokens for every agent.
 
     Q [A, c, Hq, d]; K_base, V_base [n0+c, Hkv, d]; L [n0+c, ldL];
     B [A, r, Hkv*d].  The query at chunk position p (absolute position n0+p)
     sees keys 0 .. n0+p inclusive.  Returns O [A, c, Hq, d] in fp64.
+    `positions` restricts the work to those chunk positions (the other rows
+    of O stay zero); it selects rows, it does not change their arithmetic.
     """
     Q, K, V, L, B = (to_f64(t) for t in (Q, K_base, V_base, L, B))
     A, c, hq, d = Q.shape
@@ -175,7 +177,7 @@ def prefill(Q, K_base, V_base, L, B, n0: int, rank: int, scale: float = None,
         Va = agent_value_cache(V, L[:, _agent_cols(a, rank, agent_stride)], B[a], hkv, d)
         for j in range(hq):
             h = j // G
-            for p in range(c):
+            for p in (range(c) if positions is None else positions):
                 vis = n0 + p + 1
                 O[a, p, j] = _softmax_attend(Q[a, p, j], K[:vis, h], Va[:vis, h], scale)
     return O
