@@ -111,8 +111,8 @@ def _dense(t: torch.Tensor, name: str):
         raise ValueError(f"{name} must be contiguous")
 
 
-# Zero-initialised workspaces, one per (device, stream): the library leaves
-# the ticket words zero after every call, so a workspace is reused as is.
+# Workspaces cached per (device, stream): calls on one stream are ordered, so
+# they can share one.
 _workspaces = {}
 
 
@@ -120,7 +120,7 @@ def _workspace(nbytes: int, device: torch.device, stream_ptr: int) -> torch.Tens
     key = (device.index, stream_ptr)
     ws = _workspaces.get(key)
     if ws is None or ws.numel() < nbytes:
-        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
         _workspaces[key] = ws
     return ws
 

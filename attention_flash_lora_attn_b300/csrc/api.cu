@@ -43,7 +43,6 @@ fla_status check_launch(const char *what) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-size_t dtype_size(int32_t dt) { return dt == FLA_F32 ? 4 : 2; }
 
 // Checks shared by decode and prefill.  Fills `scale`.
 fla_status check_dims(const fla_attn_dims *d, float *scale) {
@@ -146,7 +145,7 @@ fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, 
 // ---------------------------------------------------------------------------
 size_t flash_lora_attn_decode_workspace_size(const fla_attn_dims *dims, int32_t n_req,
                                              int64_t total_tokens) {
-  float scale;
+  float scale = 0.f;
   if (check_dims(dims, &scale) != FLA_OK || n_req < 0 || total_tokens < 0) return 0;
   if (dims->kernel == FLA_KERNEL_SIMT) return 0;
   if (!fla::decode_tc_shape_supported(*dims)) return 0;
@@ -159,7 +158,7 @@ fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, cons
                                   float *O, void *workspace, size_t workspace_bytes,
                                   fla_stream_t stream) {
   g_last_error.clear();
-  float scale;
+  float scale = 0.f;
   fla_status st = check_dims(dims, &scale);
   if (st != FLA_OK) return st;
   if (n_req < 0 || total_tokens < 0) return fail(FLA_ERR_INVALID_ARG, "n_req and total_tokens must be >= 0");
@@ -213,7 +212,7 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
                                    fla_stream_t stream) {
   (void)workspace; (void)workspace_bytes;
   g_last_error.clear();
-  float scale;
+  float scale = 0.f;
   fla_status st = check_dims(dims, &scale);
   if (st != FLA_OK) return st;
   if (n0 < 0 || chunk < 0) return fail(FLA_ERR_INVALID_ARG, "n0 and chunk must be >= 0");

@@ -2,31 +2,40 @@
 //
 // LRAgent technical summary (gist.science), Metodologia section 3: the output
 // is computed as P.V_base + (P.L_a).B_a, so the r-wide P.L_a accumulates in the
-// same pass as the d-wide P.V_base and B_a is applied once per query at the
-// end.  Section 2 (BaseShared): K_base / V_base are one cache shared by every
-// agent, so all agents' query rows of a kv head are served from one read of
-// each K/V tile (like query heads of a GQA group).
+// same pass as the d-wide P.V_base and B_a is applied once per query, after
+// the token loop.  Section 2 (BaseShared): K_base / V_base are one cache
+// shared by every agent, so all agents' query rows of a kv head are served
+// from one read of each K/V tile (like the query heads of a GQA group).
 //
 // Work decomposition.  A work item is (request q, kv head h, unit u): a
 // contiguous range of at most `unit_tokens` tokens of request q.  One CTA per
 // work item; the CTA index is unit_global * hkv + h so the kv heads of the same
 // token range run side by side and share the L tile through L2.
 //
-// Inside a CTA:
-//   * one producer warp streams token tiles of T tokens with TMA into a ring of
-//     STAGES shared-memory stages (K tile, V tile and the L tile holding every
-//     agent's r columns), 128/64/32-byte swizzled, mbarrier full/empty ring;
-//   * MT x TG consumer warps: the A*G query rows of kv head h (agent-major:
-//     row = a*G + g) are cut into MT tiles of 16 rows; warp (mt, tg) owns row
-//     tile mt and a 32-token slice tg of every stage.  S = Q.K^T, P.V_base and
-//     P.L_window run on mma.sync m16n8k16 (bf16 in, fp32 accumulate); the online
-//     softmax state (running max m, running sum l) and both accumulators stay
-//     in registers, reductions over the 4 lanes of a row quad use shuffles;
-//   * the TG token slices are merged in shared memory; a CTA that is the only
-//     unit of its (q, h) applies B and writes O, otherwise it writes its
-//     partial (m, l, P.V_base, own-agent P.L_a) to the workspace and the last
-//     CTA to arrive (atomic ticket, no waiting) merges all units of (q, h) in
-//     unit order (deterministic), applies B_a's head slice and writes O.
+// Inside a CTA (SG x MT x TG warps, no dedicated producer warp):
+//   * the A*G query rows of kv head h (agent-major: row = a*G + g) are cut into
+//     MT tiles of 16 rows; warp (sg, mt, tg) owns row tile mt and token slice
+//     tg (16 tokens) of the stages of T = 16*TG tokens that warp group sg
+//     consumes (tile i belongs to group i % SG);
+//   * lane 0 of each group's first warp streams that group's token tiles with
+//     TMA into a ring of shared-memory stages (K tile, V tile, and the L tile
+//     holding every agent's r columns; 128/64/32-byte swizzle) guarded by
+//     full/empty mbarriers, and refills a stage as soon as every warp of the
+//     group has released it;
+//   * S = Q.K^T, P.V_base and P.L_window run on mma.sync m16n8k16 (bf16 in,
+//     fp32 accumulate); the online-softmax state (running max m, running sum
+//     l) and both accumulators stay in registers, row reductions use quad
+//     shuffles; the rescale is skipped when no running max moved;
+//   * after the loop each warp adds (P.L_a).B_a to its P.V_base accumulator
+//     with mma.sync, the r-wide P.L_a split into a bf16 high and low part so
+//     the product keeps ~16 mantissa bits, rows masked to their own agent;
+//   * the SG*TG token slices are merged in shared memory; a CTA that is the only
+//     unit of its (q, h) writes O, otherwise it writes its partial
+//     (m, l, d-wide accumulator) to the workspace;
+//   * decode_merge_kernel, launched right behind with programmatic dependent
+//     launch (it waits on the grid dependency, no flag polling), combines the
+//     partials of every (q, h) in unit order (deterministic) and writes O: one
+//     warp per query row, every unit's load in flight at once.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -40,17 +49,17 @@
 namespace fla {
 namespace dec {
 
-constexpr int kTW = 32;             // tokens per consumer warp per stage
-constexpr int kMaxRows = 64;        // A*G query rows per kv head (MT <= 4)
-constexpr int kMaxUnitsPerPair = 512;
-constexpr int kSmemBudget = 200 * 1024;
+constexpr int kMaxRows = 64;         // A*G query rows per kv head (MT <= 4)
+constexpr int kMaxUnitsPerPair = 128;
+constexpr int kSmemBudget = 224 * 1024;
+constexpr int kTW = 16;              // tokens per warp per stage
 
 struct Params {
   const __nv_bfloat16 *Q, *B;
   float *O;
   const int32_t *offsets;
   float *partials;
-  uint32_t *tickets;
+  int2 *pair_info;         // per (q, head): first global unit, unit count (for the merge kernel)
   int32_t n_req, A, hq, hkv, G, r, rows;
   int32_t l_agent_stride;  // 0 or r
   int32_t l_width;         // columns of L held per token in shared memory
@@ -58,6 +67,9 @@ struct Params {
   int32_t l_swz_bytes;     // 32, 64 or 128
   int32_t unit_tokens;
   int32_t stages;
+  int32_t bs_dedicated;    // 1: B slices prefetched into their own region at kernel start
+  int32_t single_len;      // n_req == 1: tokens of the request (no offsets scan); else -1
+  int32_t part_stride;     // floats per unit partial in the workspace (multiple of 4)
   float scale_log2;        // softmax scale * log2(e)
 };
 
@@ -75,32 +87,51 @@ __device__ __forceinline__ int swz_chunk(int chunk, int row, int row_bytes) {
   return chunk ^ (((row * row_bytes) >> 7) & (row_bytes / 16 - 1));
 }
 
-template <int D, int MT, int TG, int NLT>
+// D: head_dim; MT: 16-row tiles; TG: token slices (warps) per row tile and
+// stage; NLT: 8-column n-tiles of the L window; SG: warp groups taking
+// alternate stages.
+template <int D, int MT, int TG, int NLT, int SG>
 struct Cfg {
-  static constexpr int T = TG * kTW;
-  static constexpr int kConsumerWarps = MT * TG;
-  static constexpr int kThreads = (kConsumerWarps + 1) * 32;
+  static constexpr int TW = kTW;
+  static constexpr int T = TG * TW;
+  static constexpr int kGroupWarps = MT * TG;
+  static constexpr int kWarps = kGroupWarps * SG;
+  static constexpr int kSlices = TG * SG;  // warps sharing one row tile
+  static constexpr int kThreads = kWarps * 32;
   static constexpr int kRowsPad = MT * 16;
   static constexpr int kQPitch = D * 2 + 16;  // bytes per Q row in shared memory
-  static constexpr int kLwin = NLT * 8;       // L window columns per row tile
-  // per-warp merge scratch: 16 rows x (D + kLwin) accumulators + m + l
-  static constexpr int kScratchFloats = 16 * (D + kLwin + 2);
+  // per-warp merge scratch: 16 rows x D accumulators (row pitch D + 8 against
+  // bank conflicts), then m[16], l[16]
+  static constexpr int kSPitch = D + 8;
+  static constexpr int kScratchFloats = 16 * kSPitch + 32;
 };
 
-template <int D, int MT, int TG, int NLT>
-__global__ void __launch_bounds__(Cfg<D, MT, TG, NLT>::kThreads, 1)
+__device__ __forceinline__ uint32_t pack_hi_lo(float x0, float x1, uint32_t &lo) {
+  const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+  lo = ptx::pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+  return (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+}
+
+template <int D, int MT, int TG, int NLT, int SG>
+__global__ void __launch_bounds__(Cfg<D, MT, TG, NLT, SG>::kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                 const __grid_constant__ CUtensorMap tmL, const Params p) {
-  using C = Cfg<D, MT, TG, NLT>;
+                 const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmB,
+                 const Params p) {
+  using C = Cfg<D, MT, TG, NLT, SG>;
+  constexpr int TW = C::TW;
   constexpr int T = C::T;
+  constexpr int kNT = C::kThreads;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const StageGeom geo{T, D, p.l_width, p.l_swz_bytes};
   const int stage_bytes = geo.stage_bytes();
-  uint8_t *q_smem = smem + p.stages * stage_bytes;
+  const int bs_bytes = p.A * p.r * D * 2;
+  uint8_t *bsm = smem + p.stages * stage_bytes;  // dedicated B region (when bs_dedicated)
+  uint8_t *q_smem = bsm + (p.bs_dedicated ? bs_bytes : 0);
   uint64_t *bars = reinterpret_cast<uint64_t *>(q_smem + C::kRowsPad * C::kQPitch);
-  __shared__ int s_info[8];   // q, unit, n_units, token begin, token count, valid
-  __shared__ int s_flag[2];   // [0] abort, [1] last-arrival
+  // bars: full[stages] | empty[stages] | B loaded | merge batch
+  __shared__ int s_info[8];   // q, unit, n_units, token begin, token count, found
+  __shared__ int s_flag[1];   // abort
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x % p.hkv;
@@ -110,6 +141,18 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (warp == 0) {
     int base = 0, found = 0;
     const int U = p.unit_tokens;
+    if (p.single_len >= 0) {  // one request: its length is known, no scan
+      const int len = p.single_len;
+      const int nu = len > 0 ? (len + U - 1) / U : 1;
+      found = unit_global < nu;
+      if (found && lane == 0) {
+        s_info[0] = 0;
+        s_info[1] = unit_global;
+        s_info[2] = nu;
+        s_info[3] = unit_global * U;
+        s_info[4] = len > 0 ? min(U, len - unit_global * U) : 0;
+      }
+    }
     for (int q0 = 0; q0 < p.n_req && !found; q0 += 32) {
       const int q = q0 + lane;
       int len = 0, nu = 0;
@@ -125,16 +168,14 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       }
       const int excl = base + incl - nu;
       const bool mine = (q < p.n_req) && unit_global >= excl && unit_global < excl + nu;
-      const unsigned m = __ballot_sync(0xffffffffu, mine);
-      if (m) {
+      if (__ballot_sync(0xffffffffu, mine)) {
         found = 1;
         if (mine) {
           const int u = unit_global - excl;
-          const int tb = p.offsets[q] + u * U;
           s_info[0] = q;
           s_info[1] = u;
           s_info[2] = nu;
-          s_info[3] = tb;
+          s_info[3] = p.offsets[q] + u * U;
           s_info[4] = len > 0 ? min(U, len - u * U) : 0;
         }
       }
@@ -143,75 +184,73 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) {
       s_info[5] = found;
       s_flag[0] = 0;
-      s_flag[1] = 0;
+      for (int s = 0; s < p.stages; ++s) {
+        ptx::mbar_init(ptx::smem_u32(&bars[s]), 1);                   // full: one arrive + tx bytes
+        ptx::mbar_init(ptx::smem_u32(&bars[p.stages + s]), C::kGroupWarps);  // empty: one arrive per warp of the group
+      }
+      ptx::mbar_init(ptx::smem_u32(&bars[2 * p.stages]), 1);      // B slices loaded
+      ptx::mbar_init(ptx::smem_u32(&bars[2 * p.stages + 1]), 1);  // merge batch loaded
+      ptx::fence_mbar_init();
     }
-  }
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      ptx::mbar_init(ptx::smem_u32(&bars[s]), 1);                         // full: producer arrive + tx
-      ptx::mbar_init(ptx::smem_u32(&bars[p.stages + s]), C::kConsumerWarps);  // empty
-    }
-    ptx::fence_mbar_init();
   }
   __syncthreads();
+  // the merge kernel behind this one may be scheduled now; it still waits for
+  // this grid to finish before reading the partials
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!s_info[5]) return;  // grid slack beyond the last unit
   const int q = s_info[0], unit = s_info[1], n_units = s_info[2];
   const int tok_begin = s_info[3], n_tok = s_info[4];
+  // every (q, head) tells the merge kernel where its units start and how many
+  // there are (the workspace is not initialised; single-unit pairs are skipped)
+  if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(unit_global, n_units);
   const int n_tiles = (n_tok + T - 1) / T;
   const uint32_t bar_full0 = ptx::smem_u32(&bars[0]);
   const uint32_t bar_empty0 = ptx::smem_u32(&bars[p.stages]);
+  const int grp = warp / C::kGroupWarps;  // warp group: consumes tiles grp, grp + SG, ...
+  const bool producer = (threadIdx.x == grp * C::kGroupWarps * 32);
+  const int n_lbox = p.l_width / p.l_box_cols;
+  const int lbox_bytes = T * p.l_swz_bytes;
 
-  if (warp == C::kConsumerWarps) {
-    // ======================= producer warp =======================
-    if (lane == 0) {
-      ptx::prefetch_tmap(&tmK);
-      ptx::prefetch_tmap(&tmV);
-      ptx::prefetch_tmap(&tmL);
-      const int n_lbox = p.l_width / p.l_box_cols;
-      const int lbox_bytes = T * p.l_swz_bytes;
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % p.stages;
-        const uint32_t ph = (it / p.stages) & 1;
-        if (it >= p.stages) {
-          if (!ptx::mbar_wait(bar_empty0 + 8 * st, ph ^ 1)) {
-            set_device_error(kErrDecodeEmptyWait);
-            s_flag[0] = 1;
-            break;
-          }
-        }
-        if (*(volatile int *)&s_flag[0]) break;
-        const uint32_t fb = bar_full0 + 8 * st;
-        ptx::mbar_arrive_expect_tx(fb, stage_bytes);
-        const uint32_t sbase = ptx::smem_u32(smem + st * stage_bytes);
-        const int tok = tok_begin + it * T;
+  auto issue_tile = [&](int it) {
+    const int st = it % p.stages;
+    const uint32_t fb = bar_full0 + 8 * st;
+    ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+    const uint32_t sbase = ptx::smem_u32(smem + st * stage_bytes);
+    const int tok = tok_begin + it * T;
 #pragma unroll
-        for (int b = 0; b < D / 64; ++b) {
-          ptx::tma_load_3d(sbase + b * T * 128, &tmK, b * 64, head, tok, fb);
-          ptx::tma_load_3d(sbase + geo.k_bytes() + b * T * 128, &tmV, b * 64, head, tok, fb);
-        }
-        for (int b = 0; b < n_lbox; ++b)
-          ptx::tma_load_2d(sbase + 2 * geo.k_bytes() + b * lbox_bytes, &tmL, b * p.l_box_cols, tok, fb);
-        ++issued;
-      }
-      // Do not leave while copies are in flight: wait (bounded) for the last
-      // load issued into each stage.
-      for (int k = 0; k < p.stages && k < issued; ++k) {
-        const int it = issued - 1 - k;
-        const int st = it % p.stages;
-        if (!ptx::mbar_wait(bar_full0 + 8 * st, (it / p.stages) & 1)) set_device_error(kErrDecodeFullWait);
-      }
+    for (int b = 0; b < D / 64; ++b) {
+      ptx::tma_load_3d(sbase + b * T * 128, &tmK, b * 64, head, tok, fb);
+      ptx::tma_load_3d(sbase + geo.k_bytes() + b * T * 128, &tmV, b * 64, head, tok, fb);
     }
-    return;  // the producer takes no part in the epilogue
+    for (int b = 0; b < n_lbox; ++b)
+      ptx::tma_load_2d(sbase + 2 * geo.k_bytes() + b * lbox_bytes, &tmL, b * p.l_box_cols, tok, fb);
+  };
+  // B_a[:, h*d:(h+1)*d] of every agent: boxes of 16 rows x 64 columns, 128B swizzle
+  const uint32_t bar_b = ptx::smem_u32(&bars[2 * p.stages]);
+  auto issue_B = [&](uint32_t dst) {
+    ptx::mbar_arrive_expect_tx(bar_b, bs_bytes);
+    for (int kc = 0; kc < p.A * p.r / 16; ++kc)
+#pragma unroll
+      for (int b = 0; b < D / 64; ++b)
+        ptx::tma_load_2d(dst + (kc * (D / 64) + b) * 2048, &tmB, head * D + b * 64, kc * 16, bar_b);
+  };
+  int last_issued = -1;  // meaningful in the producer threads only
+  if (producer) {
+    ptx::prefetch_tmap(&tmK);
+    ptx::prefetch_tmap(&tmV);
+    ptx::prefetch_tmap(&tmL);
+    for (int it = grp; it < p.stages && it < n_tiles; it += SG) {
+      issue_tile(it);
+      last_issued = it;
+    }
+    if (p.bs_dedicated && grp == 0) issue_B(ptx::smem_u32(bsm));
   }
 
-  // ======================= consumer warps =======================
-  constexpr int kConsumerThreads = C::kConsumerWarps * 32;
-  const int mt = warp / TG, tg = warp % TG;
+  const int mt = (warp % C::kGroupWarps) / TG, tg = warp % TG;
   const int g = lane >> 2, t4 = lane & 3;
 
   // Q rows of this kv head into shared memory (zero rows beyond A*G).
-  for (int e = threadIdx.x; e < C::kRowsPad * (D / 8); e += kConsumerThreads) {
+  for (int e = threadIdx.x; e < C::kRowsPad * (D / 8); e += kNT) {
     const int row = e / (D / 8), c8 = e % (D / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
     if (row < p.rows) {
@@ -220,7 +259,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     *reinterpret_cast<uint4 *>(q_smem + row * C::kQPitch + c8 * 16) = v;
   }
-  ptx::named_bar_sync(1, kConsumerThreads);
+  __syncthreads();
   uint32_t qf[D / 16][4];
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
@@ -236,8 +275,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int a_hi = row_hi >= row_lo ? row_hi / p.G : a_lo;
   const int c_lo = a_lo * p.l_agent_stride;
   const int win = (a_hi - a_lo) * p.l_agent_stride + p.r;  // columns actually used
-  const int lbox_bytes = T * p.l_swz_bytes;
-  const int lbox_cols = p.l_box_cols;
 
   float acc_v[D / 8][4];
   float acc_l[NLT][4];
@@ -249,28 +286,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const float sl2 = p.scale_log2;
   bool aborted = false;
 
-  for (int it = 0; it < n_tiles; ++it) {
+  for (int it = grp; it < n_tiles; it += SG) {
     const int st = it % p.stages;
     if (!ptx::mbar_wait(bar_full0 + 8 * st, (it / p.stages) & 1)) {
       set_device_error(kErrDecodeFullWait);
-      s_flag[0] = 1;
       aborted = true;
       break;
     }
-    const uint8_t *sK = smem + st * stage_bytes;
-    const uint8_t *sV = sK + geo.k_bytes();
-    const uint8_t *sL = sK + 2 * geo.k_bytes();
-    const uint32_t aK = ptx::smem_u32(sK), aV = ptx::smem_u32(sV), aL = ptx::smem_u32(sL);
-    const int tok0 = tg * kTW;  // first token of this warp's slice within the tile
+    const uint32_t aK = ptx::smem_u32(smem + st * stage_bytes);
+    const uint32_t aV = aK + geo.k_bytes();
+    const uint32_t aL = aK + 2 * geo.k_bytes();
+    const int tok0 = tg * TW;  // first token of this warp's slice within the tile
 
-    // ---- S = Q . K^T  (16 rows x 32 tokens)
-    float s[kTW / 8][4];
+    // ---- S = Q . K^T  (16 rows x TW tokens)
+    float s[TW / 8][4];
 #pragma unroll
-    for (int i = 0; i < kTW / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+    for (int i = 0; i < TW / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
 #pragma unroll
-      for (int np = 0; np < kTW / 16; ++np) {
+      for (int np = 0; np < TW / 16; ++np) {
         const int mi = lane >> 3, ri = lane & 7;
         const int tok = tok0 + np * 16 + (mi >> 1) * 8 + ri;
         const int c16 = kk * 2 + (mi & 1);
@@ -283,9 +318,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     // ---- mask tokens past the end of this unit (last tile only)
     const int valid = n_tok - it * T - tok0;  // tokens of this slice that exist
-    if (valid < kTW) {
+    if (valid < TW) {
 #pragma unroll
-      for (int nt = 0; nt < kTW / 8; ++nt) {
+      for (int nt = 0; nt < TW / 8; ++nt) {
         const int c = nt * 8 + 2 * t4;
         if (c >= valid) { s[nt][0] = -INFINITY; s[nt][2] = -INFINITY; }
         if (c + 1 >= valid) { s[nt][1] = -INFINITY; s[nt][3] = -INFINITY; }
@@ -294,7 +329,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     // ---- online softmax (log2 domain)
     float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-    for (int nt = 0; nt < kTW / 8; ++nt) {
+    for (int nt = 0; nt < TW / 8; ++nt) {
       s[nt][0] *= sl2; s[nt][1] *= sl2; s[nt][2] *= sl2; s[nt][3] *= sl2;
       mx0 = fmaxf(mx0, fmaxf(s[nt][0], s[nt][1]));
       mx1 = fmaxf(mx1, fmaxf(s[nt][2], s[nt][3]));
@@ -310,10 +345,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     const float corr0 = ptx::ex2(m0 - ref0), corr1 = ptx::ex2(m1 - ref1);
     m0 = mn0;
     m1 = mn1;
-    uint32_t pa[kTW / 16][4];
+    uint32_t pa[TW / 16][4];
     float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
-    for (int nt = 0; nt < kTW / 8; ++nt) {
+    for (int nt = 0; nt < TW / 8; ++nt) {
       const float p0 = ptx::ex2(s[nt][0] - ref0), p1 = ptx::ex2(s[nt][1] - ref0);
       const float p2 = ptx::ex2(s[nt][2] - ref1), p3 = ptx::ex2(s[nt][3] - ref1);
       rs0 += p0 + p1;
@@ -323,17 +358,20 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     l0 = l0 * corr0 + rs0;
     l1 = l1 * corr1 + rs1;
+    // rescale only when some row's running max moved (rare after the first tiles)
+    if (__any_sync(0xffffffffu, corr0 != 1.f || corr1 != 1.f)) {
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      acc_v[i][0] *= corr0; acc_v[i][1] *= corr0; acc_v[i][2] *= corr1; acc_v[i][3] *= corr1;
-    }
+      for (int i = 0; i < D / 8; ++i) {
+        acc_v[i][0] *= corr0; acc_v[i][1] *= corr0; acc_v[i][2] *= corr1; acc_v[i][3] *= corr1;
+      }
 #pragma unroll
-    for (int i = 0; i < NLT; ++i) {
-      acc_l[i][0] *= corr0; acc_l[i][1] *= corr0; acc_l[i][2] *= corr1; acc_l[i][3] *= corr1;
+      for (int i = 0; i < NLT; ++i) {
+        acc_l[i][0] *= corr0; acc_l[i][1] *= corr0; acc_l[i][2] *= corr1; acc_l[i][3] *= corr1;
+      }
     }
     // ---- acc_v += P . V_base ; acc_l += P . L_window
 #pragma unroll
-    for (int ks = 0; ks < kTW / 16; ++ks) {
+    for (int ks = 0; ks < TW / 16; ++ks) {
       const int mi = lane >> 3, ri = lane & 7;
       const int tok = tok0 + ks * 16 + (mi & 1) * 8 + ri;
 #pragma unroll
@@ -351,8 +389,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         int c8 = (c_lo >> 3) + lp * 2 + (mi >> 1);  // 8-column chunk within the L row
         if (c8 * 8 >= p.l_width) c8 = 0;            // chunk past the tile: read a valid one, unused
         const int cb = c8 * 8;
-        const int box = cb / lbox_cols;
-        const int chunk = (cb % lbox_cols) >> 3;
+        const int box = cb / p.l_box_cols;
+        const int chunk = (cb % p.l_box_cols) >> 3;
         const uint32_t addr = aL + box * lbox_bytes + tok * p.l_swz_bytes +
                               (swz_chunk(chunk, tok, p.l_swz_bytes) << 4);
         uint32_t lb[4];
@@ -363,7 +401,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bar_empty0 + 8 * st);
+    // ---- refill: once every warp of the group has released this stage, load
+    //      tile it + stages (the same group's, as stages % SG == 0)
+    if (producer && it + p.stages < n_tiles) {
+      if (!ptx::mbar_wait(bar_empty0 + 8 * st, (it / p.stages) & 1)) {
+        set_device_error(kErrDecodeEmptyWait);
+        aborted = true;
+        break;
+      }
+      issue_tile(it + p.stages);
+      last_issued = it + p.stages;
+    }
   }
+  if (aborted) s_flag[0] = 1;
 
   // ---- row sums across the quad
   l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
@@ -371,153 +421,219 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
   l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
-  // All consumers are past every full-barrier wait, so every TMA write into
-  // the stage ring has landed: the ring is reused as merge scratch.
-  ptx::named_bar_sync(1, kConsumerThreads);
-  if (*(volatile int *)&s_flag[0] || aborted) return;
+  __syncthreads();
+  if (s_flag[0]) {
+    // Do not leave while copies are in flight: wait (bounded) for the last
+    // load issued into each stage.
+    if (producer) {
+      for (int it = last_issued; it >= 0 && it > last_issued - p.stages; it -= SG)
+        ptx::mbar_wait(bar_full0 + 8 * (it % p.stages), (it / p.stages) & 1);
+      if (p.bs_dedicated && grp == 0) ptx::mbar_wait(bar_b, 0);
+    }
+    return;
+  }
+  // Every issued tile was waited on by every warp, so no TMA write is pending:
+  // the stage ring is reused below.
 
-  float *scratch = reinterpret_cast<float *>(smem) + warp * C::kScratchFloats;
-  // layout per warp: [16][D] acc_v | [16][kLwin] acc_l | [16] m | [16] l
+  // ---- B slices: prefetched at the start, or loaded now into the free ring
+  uint8_t *bs = p.bs_dedicated ? bsm : smem;
+  if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
+  if (!ptx::mbar_wait(bar_b, 0)) {
+    set_device_error(kErrDecodeFullWait);
+    return;  // the only copy in flight is the one that never completed
+  }
+
+  // ---- acc_v += (P.L_a) . B_a for this warp's rows (K = window columns of agent a)
   {
-    float *sv = scratch, *sl = scratch + 16 * D, *sm = sl + 16 * C::kLwin, *ss = sm + 16;
+    const int rowg0 = row_lo + g, rowg1 = row_lo + g + 8;
+    const int ag0 = rowg0 < p.rows ? rowg0 / p.G : -1;
+    const int ag1 = rowg1 < p.rows ? rowg1 / p.G : -1;
+#pragma unroll
+    for (int ks = 0; ks < NLT / 2; ++ks) {
+      if (ks * 16 >= win) break;  // warp-uniform
+      for (int a = a_lo; a <= a_hi; ++a) {
+        const int blk = a * p.l_agent_stride - c_lo;      // agent a's first window column
+        if (ks * 16 < blk || ks * 16 >= blk + p.r) continue;  // this k-step is not agent a's
+        const int kb = ks * 16 - blk;                      // first row of B_a for this k-step
+        const bool own0 = (ag0 == a), own1 = (ag1 == a);
+        uint32_t ah[4], al[4];
+        ah[0] = pack_hi_lo(own0 ? acc_l[2 * ks][0] : 0.f, own0 ? acc_l[2 * ks][1] : 0.f, al[0]);
+        ah[1] = pack_hi_lo(own1 ? acc_l[2 * ks][2] : 0.f, own1 ? acc_l[2 * ks][3] : 0.f, al[1]);
+        ah[2] = pack_hi_lo(own0 ? acc_l[2 * ks + 1][0] : 0.f, own0 ? acc_l[2 * ks + 1][1] : 0.f, al[2]);
+        ah[3] = pack_hi_lo(own1 ? acc_l[2 * ks + 1][2] : 0.f, own1 ? acc_l[2 * ks + 1][3] : 0.f, al[3]);
+        const int mi = lane >> 3, ri = lane & 7;
+        const int rr = (mi & 1) * 8 + ri;                 // row within the 16-row box
+        const int kc = (a * p.r + kb) >> 4;               // 16-row box index
+        const uint32_t bbox = ptx::smem_u32(bs) + kc * (D / 64) * 2048 + rr * 128;
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          const int c16 = dp * 2 + (mi >> 1);
+          uint32_t bb[4];
+          ptx::ldsm_x4_t(bbox + (c16 >> 3) * 2048 + (swz_chunk(c16 & 7, rr, 128) << 4), bb);
+          ptx::mma_bf16(acc_v[2 * dp], ah, bb[0], bb[1]);
+          ptx::mma_bf16(acc_v[2 * dp + 1], ah, bb[2], bb[3]);
+          ptx::mma_bf16(acc_v[2 * dp], al, bb[0], bb[1]);
+          ptx::mma_bf16(acc_v[2 * dp + 1], al, bb[2], bb[3]);
+        }
+      }
+    }
+  }
+  __syncthreads();  // every warp is done with the staged B before scratch reuses it
+
+  // ---- per-warp state to scratch: [16][D] accumulator | m[16] | l[16]
+  float *fsm = reinterpret_cast<float *>(smem);
+  {
+    constexpr int SP = C::kSPitch;
+    float *sv = fsm + warp * C::kScratchFloats, *sm = sv + 16 * SP, *ss = sm + 16;
 #pragma unroll
     for (int i = 0; i < D / 8; ++i) {
       const int c = i * 8 + 2 * t4;
-      sv[g * D + c] = acc_v[i][0];
-      sv[g * D + c + 1] = acc_v[i][1];
-      sv[(g + 8) * D + c] = acc_v[i][2];
-      sv[(g + 8) * D + c + 1] = acc_v[i][3];
-    }
-#pragma unroll
-    for (int i = 0; i < NLT; ++i) {
-      const int c = i * 8 + 2 * t4;
-      sl[g * C::kLwin + c] = acc_l[i][0];
-      sl[g * C::kLwin + c + 1] = acc_l[i][1];
-      sl[(g + 8) * C::kLwin + c] = acc_l[i][2];
-      sl[(g + 8) * C::kLwin + c + 1] = acc_l[i][3];
+      *reinterpret_cast<float2 *>(sv + g * SP + c) = make_float2(acc_v[i][0], acc_v[i][1]);
+      *reinterpret_cast<float2 *>(sv + (g + 8) * SP + c) = make_float2(acc_v[i][2], acc_v[i][3]);
     }
     if (t4 == 0) {
       sm[g] = m0; sm[g + 8] = m1;
       ss[g] = l0; ss[g + 8] = l1;
     }
   }
-  ptx::named_bar_sync(1, kConsumerThreads);
+  __syncthreads();
 
-  // ---- merge the TG token slices: combined state per valid row
-  const int D_ = D, r = p.r;
-  float *cmb = reinterpret_cast<float *>(smem) + C::kConsumerWarps * C::kScratchFloats;
-  // layout: [rows][D] v | [rows][r] L(own agent) | [rows] m | [rows] l | [rows][TG] w
-  float *cv = cmb, *cl = cv + p.rows * D_, *cm = cl + p.rows * r, *cs = cm + p.rows, *cw = cs + p.rows;
-  for (int row = threadIdx.x; row < p.rows; row += kConsumerThreads) {
-    const int rt = row / 16, rr = row % 16;
+  // ---- merge the SG*TG token slices of each row tile:
+  //      mv [rows][D] | mm [rows] | ml [rows] | tw [rows][kSlices]
+  constexpr int NS = C::kSlices;
+  constexpr int SP = C::kSPitch;
+  float *mv = fsm + C::kWarps * C::kScratchFloats;
+  float *mm = mv + p.rows * D;
+  float *ml = mm + p.rows;
+  float *tw = ml + p.rows;
+  auto slice_warp = [&](int rt, int k) {  // k-th warp (over groups and slices) of row tile rt
+    return (k / TG) * C::kGroupWarps + rt * TG + (k % TG);
+  };
+  for (int row = threadIdx.x; row < p.rows; row += kNT) {
+    const int rt = row >> 4, rr = row & 15;
     float M = -INFINITY;
-    for (int k = 0; k < TG; ++k) {
-      const float *sc = reinterpret_cast<float *>(smem) + (rt * TG + k) * C::kScratchFloats;
-      M = fmaxf(M, sc[16 * D + 16 * C::kLwin + rr]);
-    }
+#pragma unroll
+    for (int k = 0; k < NS; ++k) M = fmaxf(M, fsm[slice_warp(rt, k) * C::kScratchFloats + 16 * SP + rr]);
     float lsum = 0.f;
-    for (int k = 0; k < TG; ++k) {
-      const float *sc = reinterpret_cast<float *>(smem) + (rt * TG + k) * C::kScratchFloats;
-      const float mk = sc[16 * D + 16 * C::kLwin + rr];
-      const float w = (mk == -INFINITY) ? 0.f : ptx::ex2(mk - M);
-      cw[row * TG + k] = w;
-      lsum += w * sc[16 * D + 16 * C::kLwin + 16 + rr];
+#pragma unroll
+    for (int k = 0; k < NS; ++k) {
+      const float *sc = fsm + slice_warp(rt, k) * C::kScratchFloats + 16 * SP;
+      const float w = (sc[rr] == -INFINITY) ? 0.f : ptx::ex2(sc[rr] - M);
+      tw[row * NS + k] = w;
+      lsum += w * sc[16 + rr];
     }
-    cm[row] = M;
-    cs[row] = lsum;
+    mm[row] = M;
+    ml[row] = lsum;
   }
-  ptx::named_bar_sync(1, kConsumerThreads);
-  for (int e = threadIdx.x; e < p.rows * (D_ + r); e += kConsumerThreads) {
-    const int row = e / (D_ + r), c = e % (D_ + r);
-    const int rt = row / 16, rr = row % 16;
+  __syncthreads();
+  for (int e = threadIdx.x; e < p.rows * D; e += kNT) {
+    const int row = e / D, c = e % D;
+    const int rt = row >> 4, rr = row & 15;
     float v = 0.f;
-    if (c < D_) {
-      for (int k = 0; k < TG; ++k) {
-        const float *sc = reinterpret_cast<float *>(smem) + (rt * TG + k) * C::kScratchFloats;
-        v += cw[row * TG + k] * sc[rr * D + c];
-      }
-      cv[row * D_ + c] = v;
-    } else {
-      const int kcol = c - D_;
-      const int a = row / p.G;
-      const int wc = a * p.l_agent_stride - (rt * 16 / p.G) * p.l_agent_stride + kcol;  // window column
-      for (int k = 0; k < TG; ++k) {
-        const float *sc = reinterpret_cast<float *>(smem) + (rt * TG + k) * C::kScratchFloats;
-        v += cw[row * TG + k] * sc[16 * D + rr * C::kLwin + wc];
-      }
-      cl[row * r + kcol] = v;
-    }
+#pragma unroll
+    for (int k = 0; k < NS; ++k) v += tw[row * NS + k] * fsm[slice_warp(rt, k) * C::kScratchFloats + rr * SP + c];
+    mv[e] = v;
   }
-  ptx::named_bar_sync(1, kConsumerThreads);
+  __syncthreads();
 
-  const int pair = q * p.hkv + head;
-  const int part_floats = p.rows * (D_ + r + 2);
   if (n_units > 1) {
-    // ---- publish this unit's partial; the last unit of (q, head) merges
-    float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * part_floats;
-    for (int e = threadIdx.x; e < part_floats; e += kConsumerThreads) dst[e] = cmb[e];
-    __threadfence();
-    ptx::named_bar_sync(1, kConsumerThreads);
-    if (threadIdx.x == 0) {
-      const uint32_t old = atomicAdd(&p.tickets[pair], 1u);
-      s_flag[1] = (old == (uint32_t)(n_units - 1));
-    }
-    ptx::named_bar_sync(1, kConsumerThreads);
-    if (!s_flag[1]) return;
-    __threadfence();
-    // weights per (row, unit) into the (now free) merge scratch
-    const int ug0 = unit_global - unit;  // first unit of this request
-    float *wts = reinterpret_cast<float *>(smem);
-    float *msum = wts + p.rows * n_units;
-    for (int row = threadIdx.x; row < p.rows; row += kConsumerThreads) {
-      float M = -INFINITY;
-      for (int u = 0; u < n_units; ++u) {
-        const float *src = p.partials + ((int64_t)(ug0 + u) * p.hkv + head) * part_floats;
-        M = fmaxf(M, __ldcg(src + p.rows * (D_ + r) + row));
-      }
-      float lsum = 0.f;
-      for (int u = 0; u < n_units; ++u) {
-        const float *src = p.partials + ((int64_t)(ug0 + u) * p.hkv + head) * part_floats;
-        const float mu = __ldcg(src + p.rows * (D_ + r) + row);
-        const float w = (mu == -INFINITY) ? 0.f : ptx::ex2(mu - M);
-        wts[row * n_units + u] = w;
-        lsum += w * __ldcg(src + p.rows * (D_ + r) + p.rows + row);
-      }
-      msum[row] = lsum;
-    }
-    ptx::named_bar_sync(1, kConsumerThreads);
-    float *cv2 = msum + p.rows;  // merged [rows][D] v | [rows][r] L
-    for (int e = threadIdx.x; e < p.rows * (D_ + r); e += kConsumerThreads) {
-      const int row = (e < p.rows * D_) ? e / D_ : (e - p.rows * D_) / r;
-      float v = 0.f;
-      for (int u = 0; u < n_units; ++u) {
-        const float *src = p.partials + ((int64_t)(ug0 + u) * p.hkv + head) * part_floats;
-        v += wts[row * n_units + u] * __ldcg(src + e);
-      }
-      cv2[e] = v;
-    }
-    if (threadIdx.x == 0) p.tickets[pair] = 0;  // leave the workspace zeroed for the next call
-    ptx::named_bar_sync(1, kConsumerThreads);
-    cv = cv2;
-    cl = cv2 + p.rows * D_;
-    cs = msum;
+    // ---- publish this unit's partial: [rows][D] | m[rows] | l[rows], contiguous
+    //      in shared memory; the merge kernel combines the units
+    float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;
+    const float4 *src4 = reinterpret_cast<const float4 *>(mv);
+    const int n4 = p.rows * (D + 2) / 4;
+    for (int e = threadIdx.x; e < n4; e += kNT) reinterpret_cast<float4 *>(dst)[e] = src4[e];
+    for (int e = n4 * 4 + threadIdx.x; e < p.rows * (D + 2); e += kNT) dst[e] = mv[e];
+    return;
   }
 
-  // ---- epilogue: O = (P.V_base + (P.L_a) . B_a[:, h*d:(h+1)*d]) / l
-  const int64_t bstride = (int64_t)p.hkv * D_;
-  for (int e = threadIdx.x; e < p.rows * D_; e += kConsumerThreads) {
-    const int row = e / D_, c = e % D_;
+  // ---- single unit: O = (P.V_base + (P.L_a).B_a) / l
+  for (int e = threadIdx.x; e < p.rows * D; e += kNT) {
+    const int row = e / D, c = e % D;
     const int a = row / p.G, j = head * p.G + row % p.G;
-    const float lsum = cs[row];
-    float o = 0.f;
-    if (lsum > 0.f) {
-      const __nv_bfloat16 *Bc = p.B + (int64_t)a * r * bstride + (int64_t)head * D_ + c;
-      float lora = 0.f;
-      for (int k = 0; k < r; ++k) lora += cl[row * r + k] * __bfloat162float(Bc[(int64_t)k * bstride]);
-      o = (cv[row * D_ + c] + lora) / lsum;
-    }
-    p.O[(((int64_t)q * p.A + a) * p.hq + j) * D_ + c] = o;
+    const float ls = ml[row];
+    p.O[(((int64_t)q * p.A + a) * p.hq + j) * D + c] = ls > 0.f ? mv[e] / ls : 0.f;
   }
+}
+
+// ---------------------------------------------------------------------------
+// Split merge: O[q, a, j, :] = sum_u w_u acc_u / sum_u w_u l_u with
+// w_u = 2^(m_u - max_u m_u) (log2-domain running maxima), units in order.
+// Grid: (n_req * hkv, ceil(rows / 4)); one warp per query row; D/32 columns
+// per lane.  Launched with programmatic dependent launch right behind the
+// decode kernel: griddepcontrol.wait returns once that grid has completed and
+// its writes are visible.
+// ---------------------------------------------------------------------------
+struct MergeParams {
+  const float *partials;
+  const int2 *pair_info;
+  float *O;
+  int32_t n_req, A, hq, hkv, G, rows, part_stride, unit_tokens, single_len;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int pair = blockIdx.x;
+  const int q = pair / p.hkv, head = pair % p.hkv;
+  const int row = blockIdx.y * 4 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= p.rows) return;
+  int ug0, nu;
+  if (p.single_len >= 0) {
+    ug0 = 0;
+    nu = p.single_len > 0 ? (p.single_len + p.unit_tokens - 1) / p.unit_tokens : 1;
+  } else {
+    const int2 info = __ldcg(p.pair_info + pair);
+    ug0 = info.x;
+    nu = info.y;
+  }
+  if (nu <= 1) return;  // written directly by the decode kernel
+  constexpr int CPL = D / 32;  // columns per lane
+  const int64_t ustride = (int64_t)p.hkv * p.part_stride;
+  const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
+  // pass 1: the row's maximum over units
+  float M = -INFINITY;
+  for (int u = lane; u < nu; u += 32) M = fmaxf(M, __ldcg(base + u * ustride + p.rows * D + row));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // pass 2: weighted sums, eight units' loads in flight per step
+  float acc[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  float lsum = 0.f;
+  for (int u0 = 0; u0 < nu; u0 += 8) {
+    float mu[8], lu[8];
+    float v[8][CPL];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int u = min(u0 + k, nu - 1);
+      const float *src = base + u * ustride;
+      mu[k] = __ldcg(src + p.rows * D + row);
+      lu[k] = __ldcg(src + p.rows * D + p.rows + row);
+      if constexpr (CPL == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * D) + lane);
+        v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * D + lane * CPL + c);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (u0 + k < nu) {
+        const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
+        lsum += w * lu[k];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
+      }
+    }
+  }
+  const int a = row / p.G, j = head * p.G + row % p.G;
+  float *o = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) o[c] = acc[c] * inv;
 }
 
 }  // namespace dec
@@ -531,15 +647,15 @@ inline const char *&decode_tc_err() {
 }
 inline const char *decode_tc_last_error() { return decode_tc_err(); }
 inline const char *decode_tc_limits() {
-  return "bf16; head_dim 64 or 128; rank % 8 == 0; l_agent_stride 0 or rank; n_agents*hq/hkv <= 64; "
+  return "bf16; head_dim 64 or 128; rank % 16 == 0; l_agent_stride 0 or rank; n_agents*hq/hkv <= 64; "
          "L window per 16-row tile <= 128 columns; loaded L width % 16 == 0; 16-byte aligned pointers; "
          "l_row_stride % 8 == 0";
 }
 
 struct DecodePlan {
-  int D, MT, TG, NLT;
+  int D, MT, TG, NLT, SG;
   int rows, l_width, l_box_cols, l_swz;
-  int T, stages, smem_bytes;
+  int T, stages, smem_bytes, part_stride, bs_dedicated;
   bool ok;
 };
 
@@ -548,8 +664,9 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
   pl.ok = false;
   if (d.dtype != FLA_BF16) return pl;
   if (d.head_dim != 64 && d.head_dim != 128) return pl;
-  if (d.rank % 8 != 0 || d.rank > 128) return pl;
+  if (d.rank % 16 != 0 || d.rank > 128) return pl;
   if (d.l_agent_stride != 0 && d.l_agent_stride != d.rank) return pl;
+  const int D = d.head_dim, r = d.rank;
   const int G = d.hq / d.hkv;
   const int rows = d.n_agents * G;
   if (rows > dec::kMaxRows) return pl;
@@ -558,35 +675,53 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
   int wmax = 0;
   for (int mt = 0; mt < MT; ++mt) {
     const int lo = mt * 16, hi = std::min(rows, lo + 16) - 1;
-    const int w = (hi / G - lo / G) * (int)d.l_agent_stride + d.rank;
+    const int w = (hi / G - lo / G) * (int)d.l_agent_stride + r;
     wmax = std::max(wmax, w);
   }
   if (wmax > 128) return pl;
   const int NLT = wmax <= 64 ? 8 : 16;
-  const int l_width = d.l_agent_stride == 0 ? d.rank : d.n_agents * d.rank;
+  const int l_width = d.l_agent_stride == 0 ? r : d.n_agents * r;
   int swz = 0;
   if ((l_width * 2) % 128 == 0) swz = 128;
   else if ((l_width * 2) % 64 == 0) swz = 64;
   else if ((l_width * 2) % 32 == 0) swz = 32;
   else return pl;
-  const int TG = MT == 1 ? 4 : (MT == 4 ? 1 : 2);
+  // eight warps (two per scheduler) where the row tiles allow it; a single row
+  // tile uses two warp groups on alternate 64-token stages (more, smaller
+  // stages in flight than one group of eight on 128-token stages)
+  const int TG = MT <= 2 ? 4 : 2;
+  const int SG = MT == 1 ? 2 : 1;
   const int T = TG * dec::kTW;
-  const int stage = 2 * T * d.head_dim * 2 + T * l_width * 2;
-  const int q_bytes = MT * 16 * (d.head_dim * 2 + 16);
-  // merge scratch (aliases the stage ring) must fit into the ring
-  const int scratch_tg = (MT * TG * 16 * (d.head_dim + NLT * 8 + 2) + rows * (d.head_dim + d.rank + 2 + TG)) * 4;
-  // the last unit's merge: weights [rows][units] + sums [rows] + merged [rows][D + r]
-  const int scratch_units = rows * (dec::kMaxUnitsPerPair + 1 + d.head_dim + d.rank) * 4;
-  const int scratch = std::max(scratch_tg, scratch_units);
-  int stages = (dec::kSmemBudget - q_bytes - 1024 - 256) / stage;
+  const int stage = 2 * T * D * 2 + T * l_width * 2;
+  const int q_bytes = MT * 16 * (D * 2 + 16);
+  // epilogue regions (floats), aliased onto the stage ring after the main loop
+  const int scratch = MT * TG * SG * (16 * (D + 8) + 32);
+  const int tg_merge = rows * (D + 2) + ((rows * TG * SG + 3) & ~3);
+  const int part_bytes = ((rows * (D + 2) + 3) & ~3) * 4;
+  const int bs_bytes = d.n_agents * r * D * 2;
+  const int ring_min = std::max({(scratch + tg_merge) * 4, part_bytes, 2 * stage});
+  const int fixed = q_bytes + (2 * 8 + 2) * 8 + 1024;
+  // B slices get their own region (prefetched at kernel start) when that costs
+  // no stage (or at least three stages remain); otherwise they are loaded into
+  // the ring after the token loop
+  const int stages_plain = (dec::kSmemBudget - fixed) / stage;
+  int stages = (dec::kSmemBudget - fixed - bs_bytes) / stage;
+  int bs_dedicated = 1;
+  if (stages < std::min(stages_plain, 3) || stages < 2 || stages * stage < ring_min) {
+    bs_dedicated = 0;
+    stages = stages_plain;
+  }
   if (stages > 8) stages = 8;
-  while (stages >= 2 && stages * stage < scratch) ++stages;
-  if (stages < 2) return pl;
-  pl.smem_bytes = stages * stage + q_bytes + 2 * stages * 8 + 1024;
+  stages -= stages % SG;  // each group owns every SG-th stage
+  if (stages < 2) stages = 2;
+  while (stages * stage < std::max(ring_min, bs_dedicated ? 0 : bs_bytes)) stages += SG;
+  pl.smem_bytes = stages * stage + (bs_dedicated ? bs_bytes : 0) + fixed;
   if (pl.smem_bytes > 227 * 1024) return pl;
-  pl.D = d.head_dim; pl.MT = MT; pl.TG = TG; pl.NLT = NLT;
+  pl.bs_dedicated = bs_dedicated;
+  pl.D = D; pl.MT = MT; pl.TG = TG; pl.NLT = NLT; pl.SG = SG;
   pl.rows = rows; pl.l_width = l_width; pl.l_box_cols = swz / 2; pl.l_swz = swz;
   pl.T = T; pl.stages = stages;
+  pl.part_stride = (rows * (D + 2) + 3) & ~3;
   pl.ok = true;
   return pl;
 }
@@ -628,9 +763,9 @@ inline size_t decode_tc_workspace_bytes(const fla_attn_dims &d, int n_req, int64
   if (!pl.ok || n_req <= 0) return 0;
   const int64_t U = decode_unit_tokens(n_req, std::max<int64_t>(total_tokens, 1), d.hkv);
   const int64_t units = decode_max_units(n_req, total_tokens, U);
-  const size_t tickets = ((size_t)n_req * d.hkv * 4 + 255) / 256 * 256;
-  const size_t part = (size_t)units * d.hkv * pl.rows * (d.head_dim + d.rank + 2) * 4;
-  return tickets + part;
+  const size_t info = ((size_t)n_req * d.hkv * sizeof(int2) + 255) / 256 * 256;
+  const size_t part = (size_t)units * d.hkv * pl.part_stride * 4;
+  return info + part;
 }
 
 typedef CUresult (*PFN_encodeTiled)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
@@ -656,16 +791,39 @@ inline CUtensorMapSwizzle swizzle_enum(int bytes) {
                       : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
-template <int D, int MT, int TG, int NLT>
+template <int D, int MT, int TG, int NLT, int SG>
 inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, const CUtensorMap &mV,
-                                const CUtensorMap &mL, const dec::Params &prm, unsigned grid, cudaStream_t s) {
-  auto kern = dec::decode_tc_kernel<D, MT, TG, NLT>;
+                                const CUtensorMap &mL, const CUtensorMap &mB, const dec::Params &prm, unsigned grid,
+                                bool need_merge, cudaStream_t s) {
+  auto kern = dec::decode_tc_kernel<D, MT, TG, NLT, SG>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
   if (e != cudaSuccess) {
     decode_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;
   }
-  kern<<<grid, dec::Cfg<D, MT, TG, NLT>::kThreads, pl.smem_bytes, s>>>(mK, mV, mL, prm);
+  kern<<<grid, dec::Cfg<D, MT, TG, NLT, SG>::kThreads, pl.smem_bytes, s>>>(mK, mV, mL, mB, prm);
+  if (!need_merge) return FLA_OK;
+  dec::MergeParams mp{};
+  mp.partials = prm.partials;
+  mp.pair_info = prm.pair_info;
+  mp.O = prm.O;
+  mp.n_req = prm.n_req; mp.A = prm.A; mp.hq = prm.hq; mp.hkv = prm.hkv; mp.G = prm.G; mp.rows = prm.rows;
+  mp.part_stride = prm.part_stride; mp.unit_tokens = prm.unit_tokens; mp.single_len = prm.single_len;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(prm.n_req * prm.hkv), (unsigned)((prm.rows + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, dec::decode_merge_kernel<D>, mp);
+  if (e != cudaSuccess) {
+    decode_tc_err() = cudaGetErrorString(e);
+    return FLA_ERR_CUDA;
+  }
   return FLA_OK;
 }
 
@@ -685,7 +843,7 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
   }
   const int64_t U = decode_unit_tokens(n_req, total_tokens, d.hkv);
   const int64_t units = decode_max_units(n_req, total_tokens, U);
-  CUtensorMap mK, mV, mL;
+  CUtensorMap mK, mV, mL, mB;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.hkv, (cuuint64_t)total_tokens};
     const cuuint64_t strides[2] = {(cuuint64_t)d.head_dim * 2, (cuuint64_t)d.hkv * d.head_dim * 2};
@@ -715,18 +873,34 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
       return FLA_ERR_CUDA;
     }
   }
+  {
+    // B viewed as [A*r rows, hkv*d columns]; boxes of 16 rows x 64 columns
+    const cuuint64_t dims[2] = {(cuuint64_t)d.hkv * d.head_dim, (cuuint64_t)d.n_agents * d.rank};
+    const cuuint64_t strides[1] = {(cuuint64_t)d.hkv * d.head_dim * 2};
+    const cuuint32_t box[2] = {64, 16};
+    const cuuint32_t es[2] = {1, 1};
+    CUresult r4 = enc(&mB, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(B), dims, strides, box, es,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r4 != CUDA_SUCCESS) {
+      decode_tc_err() = "encoding the B tensor map failed";
+      return FLA_ERR_CUDA;
+    }
+  }
   dec::Params prm{};
   prm.Q = reinterpret_cast<const __nv_bfloat16 *>(Q);
   prm.B = reinterpret_cast<const __nv_bfloat16 *>(B);
   prm.O = O;
   prm.offsets = offsets;
-  const size_t tickets = ((size_t)n_req * d.hkv * 4 + 255) / 256 * 256;
-  prm.tickets = reinterpret_cast<uint32_t *>(workspace);
-  prm.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + tickets);
+  const size_t info = ((size_t)n_req * d.hkv * sizeof(int2) + 255) / 256 * 256;
+  prm.pair_info = reinterpret_cast<int2 *>(workspace);
+  prm.partials = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(workspace) + info);
   prm.n_req = n_req; prm.A = d.n_agents; prm.hq = d.hq; prm.hkv = d.hkv; prm.G = d.hq / d.hkv;
   prm.r = d.rank; prm.rows = pl.rows; prm.l_agent_stride = (int)d.l_agent_stride;
   prm.l_width = pl.l_width; prm.l_box_cols = pl.l_box_cols; prm.l_swz_bytes = pl.l_swz;
   prm.unit_tokens = (int)U; prm.stages = pl.stages;
+  prm.bs_dedicated = pl.bs_dedicated; prm.part_stride = pl.part_stride;
+  prm.single_len = n_req == 1 ? (int)total_tokens : -1;
   prm.scale_log2 = scale * 1.4426950408889634f;
   const int64_t grid64 = units * d.hkv;
   if (grid64 > 0x7fffffffLL) {
@@ -734,17 +908,19 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
     return FLA_ERR_UNSUPPORTED;
   }
   const unsigned grid = (unsigned)grid64;
-#define FLA_DEC_CASE(DD, MM, TT, NN)                                                     \
-  if (pl.D == DD && pl.MT == MM && pl.TG == TT && pl.NLT == NN)                          \
-    return decode_tc_run<DD, MM, TT, NN>(pl, mK, mV, mL, prm, grid, s);
-  FLA_DEC_CASE(128, 1, 4, 8) FLA_DEC_CASE(128, 1, 4, 16)
-  FLA_DEC_CASE(128, 2, 2, 8) FLA_DEC_CASE(128, 2, 2, 16)
-  FLA_DEC_CASE(128, 3, 2, 8) FLA_DEC_CASE(128, 3, 2, 16)
-  FLA_DEC_CASE(128, 4, 1, 8) FLA_DEC_CASE(128, 4, 1, 16)
-  FLA_DEC_CASE(64, 1, 4, 8) FLA_DEC_CASE(64, 1, 4, 16)
-  FLA_DEC_CASE(64, 2, 2, 8) FLA_DEC_CASE(64, 2, 2, 16)
-  FLA_DEC_CASE(64, 3, 2, 8) FLA_DEC_CASE(64, 3, 2, 16)
-  FLA_DEC_CASE(64, 4, 1, 8) FLA_DEC_CASE(64, 4, 1, 16)
+  // the merge kernel is needed unless the only request fits in one unit
+  const bool need_merge = !(n_req == 1 && total_tokens <= U);
+#define FLA_DEC_CASE(DD, MM, TT, NN, GG)                                                    \
+  if (pl.D == DD && pl.MT == MM && pl.TG == TT && pl.NLT == NN && pl.SG == GG)              \
+    return decode_tc_run<DD, MM, TT, NN, GG>(pl, mK, mV, mL, mB, prm, grid, need_merge, s);
+  FLA_DEC_CASE(128, 1, 4, 8, 2) FLA_DEC_CASE(128, 1, 4, 16, 2)
+  FLA_DEC_CASE(128, 2, 4, 8, 1) FLA_DEC_CASE(128, 2, 4, 16, 1)
+  FLA_DEC_CASE(128, 3, 2, 8, 1) FLA_DEC_CASE(128, 3, 2, 16, 1)
+  FLA_DEC_CASE(128, 4, 2, 8, 1) FLA_DEC_CASE(128, 4, 2, 16, 1)
+  FLA_DEC_CASE(64, 1, 4, 8, 2) FLA_DEC_CASE(64, 1, 4, 16, 2)
+  FLA_DEC_CASE(64, 2, 4, 8, 1) FLA_DEC_CASE(64, 2, 4, 16, 1)
+  FLA_DEC_CASE(64, 3, 2, 8, 1) FLA_DEC_CASE(64, 3, 2, 16, 1)
+  FLA_DEC_CASE(64, 4, 2, 8, 1) FLA_DEC_CASE(64, 4, 2, 16, 1)
 #undef FLA_DEC_CASE
   decode_tc_err() = "no kernel instance for this plan";
   return FLA_ERR_UNSUPPORTED;

@@ -343,7 +343,8 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": e2e_value, "unit": "queries/s",
                 "h2d_bytes_per_step": int(copies[0]["Q"].numel() * 2),
                 "d2h_bytes_per_step": int(copies[0]["O"].numel() * 4)},
-        "gpu_launches": args.steps,
+        # per step: the decode kernel and the split-merge kernel behind it
+        "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
     }
     del copies, calls, graph

@@ -127,10 +127,10 @@ FLA_API fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, v
  *   O        fp32 [n_req, A, hq, d]                         (output)
  *   workspace device scratch of at least
  *            flash_lora_attn_decode_workspace_size() bytes, 256-byte
- *            aligned.  It must be all-zero before the first call that uses it;
- *            every call leaves it in that state again, so it can be reused by
- *            later calls on the same stream (calls that overlap on the GPU
- *            must use different workspaces).
+ *            aligned, any initial contents.  It holds the per-unit partial
+ *            results of long contexts between the decode kernel and the merge
+ *            kernel the call enqueues behind it; calls that may overlap on the
+ *            GPU must use different workspaces.
  * Errors: INVALID_ARG (null pointer, hq % hkv, offsets layout on the host
  * side, strides), UNSUPPORTED (shape outside the selected kernel's limits),
  * WORKSPACE (too small), CUDA (launch failure).
