@@ -100,9 +100,10 @@ struct Cfg {
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kRowsPad = MT * 16;
   static constexpr int kQPitch = D * 2 + 16;  // bytes per Q row in shared memory
-  // per-warp merge scratch: 16 rows x D accumulators (row pitch D + 8 against
-  // bank conflicts), then m[16], l[16]
-  static constexpr int kSPitch = D + 8;
+  // per-warp merge scratch: 16 rows x (D accumulators + own agent's P.L_a,
+  // at most the window width), row pitch padded by 8 against bank
+  // conflicts, then m[16], l[16]
+  static constexpr int kSPitch = D + (NLT * 8 < 64 ? NLT * 8 : 64) + 8;
   static constexpr int kScratchFloats = 16 * kSPitch + 32;
 };
 
@@ -243,7 +244,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       issue_tile(it);
       last_issued = it;
     }
-    if (p.bs_dedicated && grp == 0) issue_B(ptx::smem_u32(bsm));
+    // B is applied here only when this CTA is the only unit of its (q, head);
+    // otherwise the merge kernel applies it once after combining the units
+    if (p.bs_dedicated && grp == 0 && n_units == 1) issue_B(ptx::smem_u32(bsm));
   }
 
   const int mt = (warp % C::kGroupWarps) / TG, tg = warp % TG;
@@ -428,13 +431,15 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (producer) {
       for (int it = last_issued; it >= 0 && it > last_issued - p.stages; it -= SG)
         ptx::mbar_wait(bar_full0 + 8 * (it % p.stages), (it / p.stages) & 1);
-      if (p.bs_dedicated && grp == 0) ptx::mbar_wait(bar_b, 0);
+      if (p.bs_dedicated && grp == 0 && n_units == 1) ptx::mbar_wait(bar_b, 0);
     }
     return;
   }
   // Every issued tile was waited on by every warp, so no TMA write is pending:
   // the stage ring is reused below.
 
+  const bool single = (n_units == 1);
+  if (single) {
   // ---- B slices: prefetched at the start, or loaded now into the free ring
   uint8_t *bs = p.bs_dedicated ? bsm : smem;
   if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
@@ -479,6 +484,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
   }
   __syncthreads();  // every warp is done with the staged B before scratch reuses it
+  }  // single
 
   // ---- per-warp state to scratch: [16][D] accumulator | m[16] | l[16]
   float *fsm = reinterpret_cast<float *>(smem);
@@ -495,15 +501,32 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       sm[g] = m0; sm[g + 8] = m1;
       ss[g] = l0; ss[g + 8] = l1;
     }
+    if (!single) {
+      // own agent's P.L_a (window columns [blk, blk + r) of each row) after D
+      const int r0w = row_lo + g, r1w = row_lo + g + 8;
+      const int blk0 = (min(r0w, p.rows - 1) / p.G - a_lo) * p.l_agent_stride;
+      const int blk1 = (min(r1w, p.rows - 1) / p.G - a_lo) * p.l_agent_stride;
+#pragma unroll
+      for (int i = 0; i < NLT; ++i) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = i * 8 + 2 * t4 + h;
+          if (c >= blk0 && c < blk0 + p.r) sv[g * SP + D + c - blk0] = acc_l[i][h];
+          if (c >= blk1 && c < blk1 + p.r) sv[(g + 8) * SP + D + c - blk1] = acc_l[i][2 + h];
+        }
+      }
+    }
   }
   __syncthreads();
 
   // ---- merge the SG*TG token slices of each row tile:
-  //      mv [rows][D] | mm [rows] | ml [rows] | tw [rows][kSlices]
+  //      mv [rows][WD] | mm [rows] | ml [rows] | tw [rows][kSlices]
+  //      WD = D (B already applied) or D + r (P.V_base | own P.L_a)
   constexpr int NS = C::kSlices;
   constexpr int SP = C::kSPitch;
+  const int WD = single ? D : D + p.r;
   float *mv = fsm + C::kWarps * C::kScratchFloats;
-  float *mm = mv + p.rows * D;
+  float *mm = mv + p.rows * WD;
   float *ml = mm + p.rows;
   float *tw = ml + p.rows;
   auto slice_warp = [&](int rt, int k) {  // k-th warp (over groups and slices) of row tile rt
@@ -526,24 +549,26 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     ml[row] = lsum;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < p.rows * D; e += kNT) {
-    const int row = e / D, c = e % D;
-    const int rt = row >> 4, rr = row & 15;
-    float v = 0.f;
+  for (int c = threadIdx.x; c < WD; c += kNT) {  // one column per thread, all rows
+    for (int row = 0; row < p.rows; ++row) {
+      const int rt = row >> 4, rr = row & 15;
+      float v = 0.f;
 #pragma unroll
-    for (int k = 0; k < NS; ++k) v += tw[row * NS + k] * fsm[slice_warp(rt, k) * C::kScratchFloats + rr * SP + c];
-    mv[e] = v;
+      for (int k = 0; k < NS; ++k) v += tw[row * NS + k] * fsm[slice_warp(rt, k) * C::kScratchFloats + rr * SP + c];
+      mv[row * WD + c] = v;
+    }
   }
   __syncthreads();
 
-  if (n_units > 1) {
-    // ---- publish this unit's partial: [rows][D] | m[rows] | l[rows], contiguous
-    //      in shared memory; the merge kernel combines the units
+  if (!single) {
+    // ---- publish this unit's partial: [rows][D + r] | m[rows] | l[rows],
+    //      contiguous in shared memory; the merge kernel combines the units
     float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;
     const float4 *src4 = reinterpret_cast<const float4 *>(mv);
-    const int n4 = p.rows * (D + 2) / 4;
+    const int nf = p.rows * (WD + 2);
+    const int n4 = nf / 4;
     for (int e = threadIdx.x; e < n4; e += kNT) reinterpret_cast<float4 *>(dst)[e] = src4[e];
-    for (int e = n4 * 4 + threadIdx.x; e < p.rows * (D + 2); e += kNT) dst[e] = mv[e];
+    for (int e = n4 * 4 + threadIdx.x; e < nf; e += kNT) dst[e] = mv[e];
     return;
   }
 
@@ -557,28 +582,43 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 }
 
 // ---------------------------------------------------------------------------
-// Split merge: O[q, a, j, :] = sum_u w_u acc_u / sum_u w_u l_u with
-// w_u = 2^(m_u - max_u m_u) (log2-domain running maxima), units in order.
-// Grid: (n_req * hkv, ceil(rows / 4)); one warp per query row; D/32 columns
-// per lane.  Launched with programmatic dependent launch right behind the
-// decode kernel: griddepcontrol.wait returns once that grid has completed and
-// its writes are visible.
+// Split merge and B epilogue.  For every (q, head) whose context was split
+// into units u with partials (m_u, l_u, acc_u = P_u.V_base, pl_u = P_u.L_a):
+//   w_u = 2^(m_u - max_u m_u)          (log2-domain running maxima)
+//   O   = (sum_u w_u acc_u + (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]) / sum_u w_u l_u
+// units combined in order (deterministic).  Grid: (n_req * hkv, ceil(rows/4)),
+// one warp per query row, D/32 columns per lane, sixteen units' loads in
+// flight per step.  Launched with programmatic dependent launch right behind
+// the decode kernel: B is staged before griddepcontrol.wait, which returns
+// once the decode grid has completed and its writes are visible.
 // ---------------------------------------------------------------------------
 struct MergeParams {
   const float *partials;
   const int2 *pair_info;
+  const __nv_bfloat16 *B;
   float *O;
-  int32_t n_req, A, hq, hkv, G, rows, part_stride, unit_tokens, single_len;
+  int32_t n_req, A, hq, hkv, G, r, rows, part_stride, unit_tokens, single_len;
 };
 
 template <int D>
 __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  extern __shared__ __align__(16) uint8_t msm[];
+  constexpr int CPL = D / 32;  // accumulator columns per lane
+  __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(msm);  // [r][D] of this row's agent
+  float *red = reinterpret_cast<float *>(msm + (size_t)p.r * D * 2);  // [4 warps][32 lanes][CPL + 4]
   const int pair = blockIdx.x;
   const int q = pair / p.hkv, head = pair % p.hkv;
-  const int row = blockIdx.y * 4 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= p.rows) return;
+  const int row = blockIdx.y;
+  const int a = row / p.G, j = head * p.G + row % p.G;
+  const int r = p.r;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // B_a[:, h*d:(h+1)*d] is an input: stage it before waiting on the decode grid
+  for (int e = threadIdx.x; e < r * (D / 8); e += 128) {
+    const int k = e / (D / 8), c8 = e - k * (D / 8);
+    reinterpret_cast<uint4 *>(Bs)[e] =
+        *reinterpret_cast<const uint4 *>(p.B + ((int64_t)(a * r + k) * p.hkv + head) * D + c8 * 8);
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   int ug0, nu;
   if (p.single_len >= 0) {
     ug0 = 0;
@@ -588,52 +628,96 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
     ug0 = info.x;
     nu = info.y;
   }
-  if (nu <= 1) return;  // written directly by the decode kernel
-  constexpr int CPL = D / 32;  // columns per lane
+  if (nu <= 1) return;  // written directly by the decode kernel (uniform over the CTA)
+  const int W = D + r;
   const int64_t ustride = (int64_t)p.hkv * p.part_stride;
   const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
-  // pass 1: the row's maximum over units
-  float M = -INFINITY;
-  for (int u = lane; u < nu; u += 32) M = fmaxf(M, __ldcg(base + u * ustride + p.rows * D + row));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  // pass 2: weighted sums, eight units' loads in flight per step
-  float acc[CPL];
+  // warp w combines units w, w + 4, ... ; eight of them in flight per step
+  float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  float lsum = 0.f;
-  for (int u0 = 0; u0 < nu; u0 += 8) {
-    float mu[8], lu[8];
-    float v[8][CPL];
+  constexpr int CH = 8;
+  for (int u0 = warp; u0 < nu; u0 += 4 * CH) {
+    float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const int u = min(u0 + k, nu - 1);
+    for (int k = 0; k < CH; ++k) {
+      const int u = min(u0 + 4 * k, nu - 1);
       const float *src = base + u * ustride;
-      mu[k] = __ldcg(src + p.rows * D + row);
-      lu[k] = __ldcg(src + p.rows * D + p.rows + row);
+      mu[k] = __ldcg(src + p.rows * W + row);
+      lu[k] = __ldcg(src + p.rows * W + p.rows + row);
       if constexpr (CPL == 4) {
-        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * D) + lane);
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * W) + lane);
         v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
       } else {
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * D + lane * CPL + c);
+        for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * W + lane * CPL + c);
       }
+      a2[k][0] = lane < r ? __ldcg(src + row * W + D + lane) : 0.f;
+      a2[k][1] = lane + 32 < r ? __ldcg(src + row * W + D + 32 + lane) : 0.f;
     }
+    float Mc = M;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      if (u0 + k < nu) {
+    for (int k = 0; k < CH; ++k)
+      if (u0 + 4 * k < nu) Mc = fmaxf(Mc, mu[k]);
+    const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
+    M = Mc;
+    lsum *= sc;
+    pl[0] *= sc;
+    pl[1] *= sc;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] *= sc;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      if (u0 + 4 * k < nu) {
         const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
         lsum += w * lu[k];
 #pragma unroll
         for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
+        pl[0] += w * a2[k][0];
+        pl[1] += w * a2[k][1];
       }
     }
   }
-  const int a = row / p.G, j = head * p.G + row % p.G;
-  float *o = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  // combine the four warps (fixed order: deterministic)
+  float *my = red + (warp * 32 + lane) * (CPL + 4);
+  my[0] = M;
+  my[1] = lsum;
+  my[2] = pl[0];
+  my[3] = pl[1];
 #pragma unroll
-  for (int c = 0; c < CPL; ++c) o[c] = acc[c] * inv;
+  for (int c = 0; c < CPL; ++c) my[4 + c] = acc[c];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) Mt = fmaxf(Mt, red[(w * 32 + lane) * (CPL + 4)]);
+  float ls = 0.f, plt[2] = {0.f, 0.f}, at[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) at[c] = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float *o = red + (w * 32 + lane) * (CPL + 4);
+    const float wt = (o[0] == -INFINITY) ? 0.f : ptx::ex2(o[0] - Mt);
+    ls += wt * o[1];
+    plt[0] += wt * o[2];
+    plt[1] += wt * o[3];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) at[c] += wt * o[4 + c];
+  }
+  // (sum_u w_u pl_u) . B_a: lane k holds pl[k] (and pl[k + 32] when r > 32)
+  float lora[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
+  const __nv_bfloat16 *bs = Bs + lane * CPL;
+  for (int k = 0; k < r; ++k) {
+    const float plk = __shfl_sync(0xffffffffu, k < 32 ? plt[0] : plt[1], k & 31);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bs[k * D + c]);
+  }
+  float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
+  const float inv = ls > 0.f ? 1.f / ls : 0.f;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) out[c] = (at[c] + lora[c]) * inv;
 }
 
 }  // namespace dec
@@ -647,7 +731,7 @@ inline const char *&decode_tc_err() {
 }
 inline const char *decode_tc_last_error() { return decode_tc_err(); }
 inline const char *decode_tc_limits() {
-  return "bf16; head_dim 64 or 128; rank % 16 == 0; l_agent_stride 0 or rank; n_agents*hq/hkv <= 64; "
+  return "bf16; head_dim 64 or 128; rank % 16 == 0 and <= 64; l_agent_stride 0 or rank; n_agents*hq/hkv <= 64; "
          "L window per 16-row tile <= 128 columns; loaded L width % 16 == 0; 16-byte aligned pointers; "
          "l_row_stride % 8 == 0";
 }
@@ -664,7 +748,7 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
   pl.ok = false;
   if (d.dtype != FLA_BF16) return pl;
   if (d.head_dim != 64 && d.head_dim != 128) return pl;
-  if (d.rank % 16 != 0 || d.rank > 128) return pl;
+  if (d.rank % 16 != 0 || d.rank > 64) return pl;
   if (d.l_agent_stride != 0 && d.l_agent_stride != d.rank) return pl;
   const int D = d.head_dim, r = d.rank;
   const int G = d.hq / d.hkv;
@@ -695,33 +779,44 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
   const int stage = 2 * T * D * 2 + T * l_width * 2;
   const int q_bytes = MT * 16 * (D * 2 + 16);
   // epilogue regions (floats), aliased onto the stage ring after the main loop
-  const int scratch = MT * TG * SG * (16 * (D + 8) + 32);
-  const int tg_merge = rows * (D + 2) + ((rows * TG * SG + 3) & ~3);
-  const int part_bytes = ((rows * (D + 2) + 3) & ~3) * 4;
+  const int scratch = MT * TG * SG * (16 * (D + std::min(NLT * 8, 64) + 8) + 32);
+  const int tg_merge = rows * (D + r + 2) + ((rows * TG * SG + 3) & ~3);
+  const int part_bytes = ((rows * (D + r + 2) + 3) & ~3) * 4;
   const int bs_bytes = d.n_agents * r * D * 2;
   const int ring_min = std::max({(scratch + tg_merge) * 4, part_bytes, 2 * stage});
   const int fixed = q_bytes + (2 * 8 + 2) * 8 + 1024;
-  // B slices get their own region (prefetched at kernel start) when that costs
-  // no stage (or at least three stages remain); otherwise they are loaded into
-  // the ring after the token loop
-  const int stages_plain = (dec::kSmemBudget - fixed) / stage;
-  int stages = (dec::kSmemBudget - fixed - bs_bytes) / stage;
-  int bs_dedicated = 1;
-  if (stages < std::min(stages_plain, 3) || stages < 2 || stages * stage < ring_min) {
+  // B slices (needed in this kernel only by single-unit contexts) get their own
+  // region, prefetched at kernel start, when that costs no stage; otherwise
+  // they are loaded into the ring after the token loop
+  auto fit = [&](bool ded, int &st, int &smem) {
+    st = (dec::kSmemBudget - fixed - (ded ? bs_bytes : 0)) / stage;
+    if (st > 8) st = 8;
+    st -= st % SG;  // each group owns every SG-th stage
+    if (st < 2) st = 2;
+    while (st * stage < std::max(ring_min, ded ? 0 : bs_bytes)) st += SG;
+    smem = st * stage + (ded ? bs_bytes : 0) + fixed;
+    return smem <= 227 * 1024;
+  };
+  int st_plain, sm_plain, st_ded, sm_ded;
+  const bool ok_plain = fit(false, st_plain, sm_plain);
+  const bool ok_ded = fit(true, st_ded, sm_ded);
+  int bs_dedicated, stages;
+  if (ok_ded && (st_ded >= st_plain || !ok_plain)) {
+    bs_dedicated = 1;
+    stages = st_ded;
+    pl.smem_bytes = sm_ded;
+  } else if (ok_plain) {
     bs_dedicated = 0;
-    stages = stages_plain;
+    stages = st_plain;
+    pl.smem_bytes = sm_plain;
+  } else {
+    return pl;
   }
-  if (stages > 8) stages = 8;
-  stages -= stages % SG;  // each group owns every SG-th stage
-  if (stages < 2) stages = 2;
-  while (stages * stage < std::max(ring_min, bs_dedicated ? 0 : bs_bytes)) stages += SG;
-  pl.smem_bytes = stages * stage + (bs_dedicated ? bs_bytes : 0) + fixed;
-  if (pl.smem_bytes > 227 * 1024) return pl;
   pl.bs_dedicated = bs_dedicated;
   pl.D = D; pl.MT = MT; pl.TG = TG; pl.NLT = NLT; pl.SG = SG;
   pl.rows = rows; pl.l_width = l_width; pl.l_box_cols = swz / 2; pl.l_swz = swz;
   pl.T = T; pl.stages = stages;
-  pl.part_stride = (rows * (D + 2) + 3) & ~3;
+  pl.part_stride = (rows * (D + r + 2) + 3) & ~3;
   pl.ok = true;
   return pl;
 }
@@ -806,13 +901,24 @@ inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, con
   dec::MergeParams mp{};
   mp.partials = prm.partials;
   mp.pair_info = prm.pair_info;
+  mp.B = prm.B;
   mp.O = prm.O;
   mp.n_req = prm.n_req; mp.A = prm.A; mp.hq = prm.hq; mp.hkv = prm.hkv; mp.G = prm.G; mp.rows = prm.rows;
+  mp.r = prm.r;
   mp.part_stride = prm.part_stride; mp.unit_tokens = prm.unit_tokens; mp.single_len = prm.single_len;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(prm.n_req * prm.hkv), (unsigned)((prm.rows + 3) / 4));
+  cfg.gridDim = dim3((unsigned)(prm.n_req * prm.hkv), (unsigned)prm.rows);
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  // this row's B slice plus the cross-warp reduction buffer
+  cfg.dynamicSmemBytes = (size_t)prm.r * D * 2 + 4 * 32 * (D / 32 + 4) * 4;
+  if (cfg.dynamicSmemBytes > 48 * 1024) {
+    e = cudaFuncSetAttribute(dec::decode_merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)cfg.dynamicSmemBytes);
+    if (e != cudaSuccess) {
+      decode_tc_err() = cudaGetErrorString(e);
+      return FLA_ERR_CUDA;
+    }
+  }
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
