@@ -126,7 +126,7 @@ fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, 
   const bool tc_ok = fla::build_tc_supported(X, ldx, A_t, L, ldl, d_model, n_cols, dtype);
   if (kernel == FLA_KERNEL_TENSOR && !tc_ok)
     return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build: shape/alignment outside the tensor-core kernel "
-                "(needs bf16, d_model %% 64 == 0, n_cols %% 16 == 0, n_cols <= 512, 16-byte alignment)");
+                "(needs bf16, d_model %% 64 == 0, n_cols %% 32 == 0, n_cols <= 512, 16-byte alignment)");
   if (tc_ok && kernel != FLA_KERNEL_SIMT) {
     fla_status st = fla::build_tc_launch(X, ldx, A_t, L, ldl, n_tokens, d_model, n_cols, s);
     if (st != FLA_OK) return fail(st, "lr_cache_build (tensor): %s", fla::build_tc_last_error());

@@ -96,7 +96,7 @@ typedef struct {
  *          other columns of a wider L are left untouched)
  *   dtype  storage type of X, A_t and L; fp32 accumulation.
  *   kernel fla_kernel.  The tensor-core path needs bf16, d_model % 64 == 0,
- *          n_cols % 16 == 0, n_cols <= 512, 16-byte aligned pointers and
+ *          n_cols % 32 == 0, n_cols <= 512, 16-byte aligned pointers and
  *          ldx, ldl multiples of 8.
  * Errors: FLA_ERR_INVALID_ARG for null pointers with n_tokens > 0, negative
  * sizes, ldx < d_model or ldl < n_cols.  n_tokens == 0 is a no-op.

@@ -233,6 +233,17 @@ def test_lr_build_small(case, kernel):
     assert _rel_l2(L, ref) <= (BUILD_RTOL_L2 if dt == "bf16" else 1e-6)
 
 
+@pytest.mark.parametrize("case", [(128, 64, 32), (300, 4096, 64), (257, 512, 320), (1000, 1024, 512), (77, 128, 96)],
+                         ids=["one-tile", "llama8b-cols", "ragged-320", "n512", "n96"])
+def test_lr_build_tensor_kernel(case):
+    """The tcgen05 GEMM itself (kernel="tensor" refuses to fall back)."""
+    n, D, N = case
+    x = make_build_inputs(n, D, 1, N, torch.bfloat16, seed=8)
+    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].t().contiguous().cuda(), kernel="tensor")
+    ref = oracle.lr_cache_build(x["X"], x["A_cat"])
+    assert _rel_l2(L.double().cpu().numpy(), ref) <= BUILD_RTOL_L2
+
+
 def test_lr_build_strided_output_leaves_other_columns():
     x = make_build_inputs(200, 512, 2, 32, torch.bfloat16, seed=6)
     L = torch.full((200, 100), 7.0, dtype=torch.bfloat16, device="cuda")
@@ -244,15 +255,15 @@ def test_lr_build_strided_output_leaves_other_columns():
 
 def test_lr_build_llama8b_chunk_full():
     x = make_build_inputs(512, 4096, 4, 16, torch.bfloat16, seed=0)
-    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].t().contiguous().cuda()).double().cpu().numpy()
-    assert _rel_l2(L, oracle.lr_cache_build(x["X"], x["A_cat"])) <= BUILD_RTOL_L2
+    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].t().contiguous().cuda(), kernel="tensor")
+    assert _rel_l2(L.double().cpu().numpy(), oracle.lr_cache_build(x["X"], x["A_cat"])) <= BUILD_RTOL_L2
 
 
 def test_lr_build_llama70b_full_size_sampled_rows():
     """131072 x 8192 . 8192 x 320 on the GPU; 4096 sampled rows against the oracle."""
     x = make_build_inputs(131072, 8192, 5, 64, torch.bfloat16, seed=0)
     dX = x["X"].cuda()
-    L = _fla().lr_cache_build(dX, x["A_cat"].t().contiguous().cuda())
+    L = _fla().lr_cache_build(dX, x["A_cat"].t().contiguous().cuda(), kernel="tensor")
     rows = np.sort(np.random.default_rng(0).choice(131072, 4096, replace=False))
     rows = np.concatenate([[0, 1], rows, [131070, 131071]])
     Ls = L[torch.from_numpy(rows).cuda()].double().cpu().numpy()
