@@ -18,6 +18,7 @@
 #include "simt_kernels.cuh"
 #include "decode_tc.cuh"
 #include "build_tc.cuh"
+#include "prefill_mma.cuh"
 
 namespace {
 
@@ -219,9 +220,18 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
   if (chunk == 0) return ok();
   if (!Q || !K_base || !V_base || !L || !B || !O)
     return fail(FLA_ERR_INVALID_ARG, "Q, K_base, V_base, L, B and O must be non-NULL");
-  if (dims->kernel == FLA_KERNEL_TENSOR)
-    return fail(FLA_ERR_UNSUPPORTED, "prefill: no tensor-core kernel for this shape yet");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool shape_tc = fla::prefill_tc_shape_supported(*dims);
+  const bool align_tc = aligned16(Q) && aligned16(K_base) && aligned16(V_base) && aligned16(L) &&
+                        aligned16(B) && aligned16(O) && (dims->l_row_stride % 8 == 0);
+  if (dims->kernel == FLA_KERNEL_TENSOR && !(shape_tc && align_tc))
+    return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside the tensor-core kernel (bf16; head_dim "
+                "64 or 128; rank %% 16 == 0 and <= 64; l_agent_stride 0 or rank; 16-byte alignment)");
+  if (shape_tc && align_tc && dims->kernel != FLA_KERNEL_SIMT) {
+    st = fla::prefill_tc_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, s);
+    if (st != FLA_OK) return fail(st, "prefill (tensor): %s", fla::prefill_tc_last_error());
+    return check_launch("prefill (tensor)");
+  }
   fla::SimtAttnParams p{};
   p.Q = Q; p.K = K_base; p.V = V_base; p.L = L; p.B = B; p.O = O; p.offsets = nullptr;
   p.l_row_stride = dims->l_row_stride; p.l_agent_stride = dims->l_agent_stride; p.n0 = n0;

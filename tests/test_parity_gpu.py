@@ -177,18 +177,24 @@ def small_prefill(A, hq, hkv, d, r, n0, c):
 
 
 PREFILL_SMALL = [(1, 4, 4, 64, 8, 0, 5), (2, 8, 2, 128, 16, 37, 70), (4, 32, 8, 128, 16, 300, 129),
-                 (3, 16, 4, 128, 32, 1, 200)]
+                 (3, 16, 4, 128, 32, 1, 200), (1, 8, 8, 64, 16, 64, 1), (5, 64, 8, 128, 64, 130, 33),
+                 (2, 4, 2, 128, 16, 0, 300)]
 
 
-@pytest.mark.parametrize("kernel", ["auto", "simt"])
+@pytest.mark.parametrize("kernel", ["tensor", "simt"])
 @pytest.mark.parametrize("case", PREFILL_SMALL, ids=[f"p{i}" for i in range(len(PREFILL_SMALL))])
 def test_prefill_small(case, kernel):
     A, hq, hkv, d, r, n0, c = case
     w = small_prefill(A, hq, hkv, d, r, n0, c)
     x = make_prefill_inputs(w, seed=2, with_X=False)
     dx = to_dev(x)
-    O = _fla().flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], n0, rank=r,
-                                       kernel=kernel)
+    try:
+        O = _fla().flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], n0, rank=r,
+                                           kernel=kernel)
+    except _fla().FlaError as e:
+        if kernel == "tensor" and e.status == 2:
+            pytest.skip("shape outside the tensor-core prefill kernel")
+        raise
     ref = oracle.prefill(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], n0=n0, rank=r)
     check_attn(O, ref, what=f"prefill {case}")
 
@@ -202,7 +208,7 @@ def test_prefill_llama8b_chunk_with_lr_build_sampled_rows():
     fla = _fla()
     fla.lr_cache_build(dx["X"], A_t, dx["L"][w.n0:])
     O = fla.flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], w.n0,
-                                    rank=w.rank).cpu()
+                                    rank=w.rank, kernel="tensor").cpu()
     # oracle: its own LR rows for the chunk (fp64 product rounded to the bf16 storage type)
     L_ref = oracle.to_f64(x["L"]).copy()
     L_ref[w.n0:] = oracle.round_to_bf16(oracle.lr_cache_build(x["X"], x["A_cat"]))
