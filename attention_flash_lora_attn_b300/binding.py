@@ -27,7 +27,7 @@ STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "F
 # Every symbol the header declares (tests check that the library exports them).
 EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
             "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
-            "fla_last_error_message", "fla_device_error", "fla_version")
+            "fla_last_error_message", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc")
 
 
 class FlaError(RuntimeError):
@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fla_device_error.restype = ctypes.c_int
         lib.fla_version.argtypes = []
         lib.fla_version.restype = ctypes.c_char_p
+        lib.flash_lora_attn_decode_noalloc.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, i64, vp, vp]
+        lib.flash_lora_attn_decode_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 

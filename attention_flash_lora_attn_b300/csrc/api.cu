@@ -8,6 +8,7 @@
 // library is one translation unit with one device error word.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -242,6 +243,67 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
   if (dims->dtype == FLA_F32) launch_simt_attn<float>(p, rows, s);
   else launch_simt_attn<__nv_bfloat16>(p, rows, s);
   return check_launch("prefill (simt)");
+}
+
+// ---------------------------------------------------------------------------
+// Decode without a caller-provided workspace.
+//
+// Some callers cannot allocate device memory when they call the library: a
+// serving loop that fixed its memory budget at start-up and must not grow it
+// (cudaMalloc also synchronises the device, which a latency-bound decode loop
+// cannot afford), or a plugin whose host framework owns every allocation and
+// hands it no scratch buffer.  For them the split-context partials live in
+// the fixed array below, part of the library image: every GPU that loads the
+// library holds these 16 MiB until the process exits.
+// ---------------------------------------------------------------------------
+static constexpr size_t kNoAllocScratchBytes = 16u << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char fla_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  In host code
+// the array's name only stands in for the symbol, so the address is asked of
+// the runtime once per device, with that device current, and cached.
+fla_status noalloc_scratch(void **out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FLA_ERR_UNSUPPORTED, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, fla_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+      return fail(FLA_ERR_CUDA, "cudaGetSymbolAddress(scratch) on device %d: %s", dev, cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return FLA_OK;
+}
+}  // namespace
+
+fla_status flash_lora_attn_decode_noalloc(const fla_attn_dims *dims, const void *Q, const void *K_base,
+                                          const void *V_base, const void *L, const void *B,
+                                          const int32_t *offsets, int32_t n_req, int64_t total_tokens, float *O,
+                                          fla_stream_t stream) {
+  g_last_error.clear();
+  if (!dims) return fail(FLA_ERR_INVALID_ARG, "dims is NULL");
+  const size_t need = flash_lora_attn_decode_workspace_size(dims, n_req, total_tokens);
+  if (need > kNoAllocScratchBytes)
+    return fail(FLA_ERR_WORKSPACE,
+                "decode_noalloc: this call needs %zu bytes of scratch, more than the fixed %zu-byte array; "
+                "use flash_lora_attn_decode with a caller-provided workspace",
+                need, kNoAllocScratchBytes);
+  void *scratch = nullptr;
+  if (need > 0) {
+    const fla_status st = noalloc_scratch(&scratch);
+    if (st != FLA_OK) return st;
+  }
+  return flash_lora_attn_decode(dims, Q, K_base, V_base, L, B, offsets, n_req, total_tokens, O, scratch,
+                                need > 0 ? kNoAllocScratchBytes : 0, stream);
 }
 
 }  // extern "C"

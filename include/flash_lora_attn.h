@@ -170,6 +170,35 @@ FLA_API fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void
                                    int32_t chunk, float *O, void *workspace,
                                    size_t workspace_bytes, fla_stream_t stream);
 
+/*
+ * flash_lora_attn_decode_noalloc - flash_lora_attn_decode without a
+ * caller-provided workspace.  The pages have no counterpart: this is a
+ * library convenience, not part of the method.
+ *
+ * For callers that cannot allocate device memory at call time (a serving
+ * loop whose memory budget is fixed at start-up, or a plugin whose host
+ * framework owns every allocation and gives it no scratch buffer).  Same
+ * arguments, layouts and results as flash_lora_attn_decode minus the
+ * workspace; the partial results of split contexts go to a 16 MiB array that
+ * is part of the library image (every GPU that loads the library holds it
+ * until the process exits).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device shares the one array; it needs no zeroing (each
+ *     call writes every scratch value before reading it) and keeps the last
+ *     call's contents.  Calls on one device that may overlap on the GPU (for
+ *     example on different streams) race on the array: serialise them, or
+ *     use flash_lora_attn_decode with a workspace per stream.
+ *   - Returns FLA_ERR_WORKSPACE when the call needs more scratch than the
+ *     array holds (flash_lora_attn_decode_workspace_size() > 16 MiB).
+ */
+FLA_API fla_status flash_lora_attn_decode_noalloc(const fla_attn_dims *dims, const void *Q, const void *K_base,
+                                                  const void *V_base, const void *L, const void *B,
+                                                  const int32_t *offsets, int32_t n_req, int64_t total_tokens,
+                                                  float *O, fla_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 FLA_API const char *fla_status_string(fla_status status);
 
