@@ -4,6 +4,7 @@ Public API (thin wrappers over the C ABI in include/flash_lora_attn.h):
   lr_cache_build(X, A_t, L=None)            L = X . A_cat for every agent at once
   flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, rank=...)
   flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0, rank=...)
+  PreparedDecode(...)                       a decode call marshalled once, one C call per step
   device_error()                            read and clear the device error word
 
 All compute runs in the library's CUDA kernels; the library must have been
@@ -13,6 +14,7 @@ from .binding import (  # noqa: F401
     EXPORTED,
     LIB_PATH,
     FlaError,
+    PreparedDecode,
     device_error,
     flash_lora_attn_decode,
     flash_lora_attn_prefill,

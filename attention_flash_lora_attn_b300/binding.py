@@ -197,6 +197,53 @@ def flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, *, rank: int,
     return O
 
 
+class PreparedDecode:
+    """A decode call marshalled once: calling it enqueues the kernels with one C call.
+
+    For serving loops that decode many times over the same buffers (the
+    queries are refreshed in place, e.g. by a host->device copy into Q):
+    validation, the dims struct, the workspace and the stream are fixed at
+    construction, so each call costs one ctypes call.  Arguments as for
+    flash_lora_attn_decode.
+    """
+
+    def __init__(self, Q, K_base, V_base, L, B, offsets, *, rank: int, l_agent_stride: Optional[int] = None,
+                 scale: Optional[float] = None, O: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, kernel: str = "auto", stream=None):
+        lib = load_library()
+        _need_cuda(Q, K_base, V_base, L, B, offsets, O, workspace)
+        for t, nm in ((Q, "Q"), (K_base, "K_base"), (V_base, "V_base"), (B, "B")):
+            _dense(t, nm)
+        if L.stride(1) != 1:
+            raise ValueError("L must have unit column stride")
+        if offsets.dtype != torch.int32 or not offsets.is_contiguous():
+            raise TypeError("offsets must be a contiguous int32 tensor")
+        R, A, hq, d = Q.shape
+        N, hkv, d2 = K_base.shape
+        if d2 != d or V_base.shape != K_base.shape:
+            raise ValueError("K_base/V_base must be [N, Hkv, d] matching Q")
+        if l_agent_stride is None:
+            l_agent_stride = rank
+        self.dims = make_dims(A, hq, hkv, d, rank, _dtype_code(Q), L.stride(0), l_agent_stride, scale, kernel)
+        self.O = O if O is not None else torch.empty((R, A, hq, d), dtype=torch.float32, device=Q.device)
+        sp = _stream_ptr(stream)
+        need = lib.flash_lora_attn_decode_workspace_size(ctypes.byref(self.dims), R, N)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=Q.device)
+        self._keep = (Q, K_base, V_base, L, B, offsets, workspace)  # keep the buffers alive
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        self._fn = lib.flash_lora_attn_decode
+        self._args = (ctypes.byref(self.dims), Q.data_ptr(), K_base.data_ptr(), V_base.data_ptr(), L.data_ptr(),
+                      B.data_ptr(), offsets.data_ptr(), R, N, self.O.data_ptr(), ws_ptr, ws_bytes, sp)
+
+    def __call__(self) -> torch.Tensor:
+        st = self._fn(*self._args)
+        if st != FLA_OK:
+            _check(st)
+        return self.O
+
+
 def flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0: int, *, rank: int,
                             l_agent_stride: Optional[int] = None, scale: Optional[float] = None,
                             O: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,

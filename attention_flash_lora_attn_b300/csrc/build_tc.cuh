@@ -271,8 +271,7 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *A_t, v
   prm.n_chunks = pl.n_chunks;
   prm.stages = pl.stages;
   prm.tmem_cols = pl.tmem_cols;
-  cudaError_t e = cudaFuncSetAttribute(bld::build_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       pl.smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(bld::build_tc_kernel), pl.smem_bytes);
   if (e != cudaSuccess) {
     build_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;

@@ -137,6 +137,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x % p.hkv;
   const int unit_global = blockIdx.x / p.hkv;
+  // Launched with programmatic dependent launch: the CTA may become resident
+  // while the previous kernel in the stream drains; nothing it wrote is read
+  // before this wait returns.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // ---- map unit_global -> (request, unit) with a warp-parallel scan
   if (warp == 0) {
@@ -439,145 +443,157 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   // the stage ring is reused below.
 
   const bool single = (n_units == 1);
-  if (single) {
-  // ---- B slices: prefetched at the start, or loaded now into the free ring
-  uint8_t *bs = p.bs_dedicated ? bsm : smem;
-  if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
-  if (!ptx::mbar_wait(bar_b, 0)) {
-    set_device_error(kErrDecodeFullWait);
-    return;  // the only copy in flight is the one that never completed
-  }
 
-  // ---- acc_v += (P.L_a) . B_a for this warp's rows (K = window columns of agent a)
-  {
-    const int rowg0 = row_lo + g, rowg1 = row_lo + g + 8;
-    const int ag0 = rowg0 < p.rows ? rowg0 / p.G : -1;
-    const int ag1 = rowg1 < p.rows ? rowg1 / p.G : -1;
-#pragma unroll
-    for (int ks = 0; ks < NLT / 2; ++ks) {
-      if (ks * 16 >= win) break;  // warp-uniform
-      for (int a = a_lo; a <= a_hi; ++a) {
-        const int blk = a * p.l_agent_stride - c_lo;      // agent a's first window column
-        if (ks * 16 < blk || ks * 16 >= blk + p.r) continue;  // this k-step is not agent a's
-        const int kb = ks * 16 - blk;                      // first row of B_a for this k-step
-        const bool own0 = (ag0 == a), own1 = (ag1 == a);
-        uint32_t ah[4], al[4];
-        ah[0] = pack_hi_lo(own0 ? acc_l[2 * ks][0] : 0.f, own0 ? acc_l[2 * ks][1] : 0.f, al[0]);
-        ah[1] = pack_hi_lo(own1 ? acc_l[2 * ks][2] : 0.f, own1 ? acc_l[2 * ks][3] : 0.f, al[1]);
-        ah[2] = pack_hi_lo(own0 ? acc_l[2 * ks + 1][0] : 0.f, own0 ? acc_l[2 * ks + 1][1] : 0.f, al[2]);
-        ah[3] = pack_hi_lo(own1 ? acc_l[2 * ks + 1][2] : 0.f, own1 ? acc_l[2 * ks + 1][3] : 0.f, al[3]);
-        const int mi = lane >> 3, ri = lane & 7;
-        const int rr = (mi & 1) * 8 + ri;                 // row within the 16-row box
-        const int kc = (a * p.r + kb) >> 4;               // 16-row box index
-        const uint32_t bbox = ptx::smem_u32(bs) + kc * (D / 64) * 2048 + rr * 128;
-#pragma unroll
-        for (int dp = 0; dp < D / 16; ++dp) {
-          const int c16 = dp * 2 + (mi >> 1);
-          uint32_t bb[4];
-          ptx::ldsm_x4_t(bbox + (c16 >> 3) * 2048 + (swz_chunk(c16 & 7, rr, 128) << 4), bb);
-          ptx::mma_bf16(acc_v[2 * dp], ah, bb[0], bb[1]);
-          ptx::mma_bf16(acc_v[2 * dp + 1], ah, bb[2], bb[3]);
-          ptx::mma_bf16(acc_v[2 * dp], al, bb[0], bb[1]);
-          ptx::mma_bf16(acc_v[2 * dp + 1], al, bb[2], bb[3]);
-        }
-      }
-    }
-  }
-  __syncthreads();  // every warp is done with the staged B before scratch reuses it
-  }  // single
-
-  // ---- per-warp state to scratch: [16][D] accumulator | m[16] | l[16]
-  float *fsm = reinterpret_cast<float *>(smem);
-  {
-    constexpr int SP = C::kSPitch;
-    float *sv = fsm + warp * C::kScratchFloats, *sm = sv + 16 * SP, *ss = sm + 16;
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      const int c = i * 8 + 2 * t4;
-      *reinterpret_cast<float2 *>(sv + g * SP + c) = make_float2(acc_v[i][0], acc_v[i][1]);
-      *reinterpret_cast<float2 *>(sv + (g + 8) * SP + c) = make_float2(acc_v[i][2], acc_v[i][3]);
-    }
-    if (t4 == 0) {
-      sm[g] = m0; sm[g + 8] = m1;
-      ss[g] = l0; ss[g + 8] = l1;
-    }
-    if (!single) {
-      // own agent's P.L_a (window columns [blk, blk + r) of each row) after D
-      const int r0w = row_lo + g, r1w = row_lo + g + 8;
-      const int blk0 = (min(r0w, p.rows - 1) / p.G - a_lo) * p.l_agent_stride;
-      const int blk1 = (min(r1w, p.rows - 1) / p.G - a_lo) * p.l_agent_stride;
-#pragma unroll
-      for (int i = 0; i < NLT; ++i) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int c = i * 8 + 2 * t4 + h;
-          if (c >= blk0 && c < blk0 + p.r) sv[g * SP + D + c - blk0] = acc_l[i][h];
-          if (c >= blk1 && c < blk1 + p.r) sv[(g + 8) * SP + D + c - blk1] = acc_l[i][2 + h];
-        }
-      }
-    }
-  }
-  __syncthreads();
-
-  // ---- merge the SG*TG token slices of each row tile:
-  //      mv [rows][WD] | mm [rows] | ml [rows] | tw [rows][kSlices]
-  //      WD = D (B already applied) or D + r (P.V_base | own P.L_a)
+  // ---- merge the SG*TG token slices of each row tile in registers: a tree
+  //      over the slices; in each round the upper half of the slices writes
+  //      its fragments (thread-linear, conflict-free) into the free ring and
+  //      the lower half combines them with its own.  Slice 0 of each row tile
+  //      ends up holding the tile's state.
   constexpr int NS = C::kSlices;
-  constexpr int SP = C::kSPitch;
-  const int WD = single ? D : D + p.r;
-  float *mv = fsm + C::kWarps * C::kScratchFloats;
-  float *mm = mv + p.rows * WD;
-  float *ml = mm + p.rows;
-  float *tw = ml + p.rows;
-  auto slice_warp = [&](int rt, int k) {  // k-th warp (over groups and slices) of row tile rt
-    return (k / TG) * C::kGroupWarps + rt * TG + (k % TG);
-  };
-  for (int row = threadIdx.x; row < p.rows; row += kNT) {
-    const int rt = row >> 4, rr = row & 15;
-    float M = -INFINITY;
+  constexpr int NV = (D / 8) * 4 + NLT * 4 + 4;  // acc_v | acc_l | m0 m1 l0 l1, per thread
+  const int kslice = grp * TG + tg;               // this warp's slice within its row tile
+  {
+    float *xch = reinterpret_cast<float *>(smem);  // [warp][NV][32 lanes]
+#pragma unroll 1
+    for (int half = NS / 2; half >= 1; half /= 2) {
+      if (kslice >= half && kslice < 2 * half) {
+        float *dst = xch + warp * NV * 32 + lane;
 #pragma unroll
-    for (int k = 0; k < NS; ++k) M = fmaxf(M, fsm[slice_warp(rt, k) * C::kScratchFloats + 16 * SP + rr]);
-    float lsum = 0.f;
+        for (int i = 0; i < D / 8; ++i)
 #pragma unroll
-    for (int k = 0; k < NS; ++k) {
-      const float *sc = fsm + slice_warp(rt, k) * C::kScratchFloats + 16 * SP;
-      const float w = (sc[rr] == -INFINITY) ? 0.f : ptx::ex2(sc[rr] - M);
-      tw[row * NS + k] = w;
-      lsum += w * sc[16 + rr];
+          for (int c = 0; c < 4; ++c) dst[(i * 4 + c) * 32] = acc_v[i][c];
+#pragma unroll
+        for (int i = 0; i < NLT; ++i)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) dst[((D / 8) * 4 + i * 4 + c) * 32] = acc_l[i][c];
+        dst[(NV - 4) * 32] = m0;
+        dst[(NV - 3) * 32] = m1;
+        dst[(NV - 2) * 32] = l0;
+        dst[(NV - 1) * 32] = l1;
+      }
+      __syncthreads();
+      if (kslice < half) {
+        const int k2 = kslice + half;
+        const int pw = (k2 / TG) * C::kGroupWarps + mt * TG + (k2 % TG);  // partner warp
+        const float *src = xch + pw * NV * 32 + lane;
+        const float pm0 = src[(NV - 4) * 32], pm1 = src[(NV - 3) * 32];
+        const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
+        const float a0 = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - M0);
+        const float b0 = (pm0 == -INFINITY) ? 0.f : ptx::ex2(pm0 - M0);
+        const float a1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - M1);
+        const float b1 = (pm1 == -INFINITY) ? 0.f : ptx::ex2(pm1 - M1);
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+          acc_v[i][0] = a0 * acc_v[i][0] + b0 * src[(i * 4 + 0) * 32];
+          acc_v[i][1] = a0 * acc_v[i][1] + b0 * src[(i * 4 + 1) * 32];
+          acc_v[i][2] = a1 * acc_v[i][2] + b1 * src[(i * 4 + 2) * 32];
+          acc_v[i][3] = a1 * acc_v[i][3] + b1 * src[(i * 4 + 3) * 32];
+        }
+#pragma unroll
+        for (int i = 0; i < NLT; ++i) {
+          const int o = (D / 8) * 4 + i * 4;
+          acc_l[i][0] = a0 * acc_l[i][0] + b0 * src[(o + 0) * 32];
+          acc_l[i][1] = a0 * acc_l[i][1] + b0 * src[(o + 1) * 32];
+          acc_l[i][2] = a1 * acc_l[i][2] + b1 * src[(o + 2) * 32];
+          acc_l[i][3] = a1 * acc_l[i][3] + b1 * src[(o + 3) * 32];
+        }
+        l0 = a0 * l0 + b0 * src[(NV - 2) * 32];
+        l1 = a1 * l1 + b1 * src[(NV - 1) * 32];
+        m0 = M0;
+        m1 = M1;
+      }
+      ptx::fence_proxy_async_smem();  // the ring may next be written by TMA (the B slices)
+      __syncthreads();
     }
-    mm[row] = M;
-    ml[row] = lsum;
   }
-  __syncthreads();
-  for (int c = threadIdx.x; c < WD; c += kNT) {  // one column per thread, all rows
-    for (int row = 0; row < p.rows; ++row) {
-      const int rt = row >> 4, rr = row & 15;
-      float v = 0.f;
-#pragma unroll
-      for (int k = 0; k < NS; ++k) v += tw[row * NS + k] * fsm[slice_warp(rt, k) * C::kScratchFloats + rr * SP + c];
-      mv[row * WD + c] = v;
-    }
-  }
-  __syncthreads();
 
-  if (!single) {
-    // ---- publish this unit's partial: [rows][D + r] | m[rows] | l[rows],
-    //      contiguous in shared memory; the merge kernel combines the units
-    float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;
-    const float4 *src4 = reinterpret_cast<const float4 *>(mv);
-    const int nf = p.rows * (WD + 2);
-    const int n4 = nf / 4;
-    for (int e = threadIdx.x; e < n4; e += kNT) reinterpret_cast<float4 *>(dst)[e] = src4[e];
-    for (int e = n4 * 4 + threadIdx.x; e < nf; e += kNT) dst[e] = mv[e];
+  const int row0 = row_lo + g, row1 = row_lo + g + 8;
+  if (single) {
+    // ---- B slices: prefetched at the start, or loaded now into the free ring
+    uint8_t *bs = p.bs_dedicated ? bsm : smem;
+    if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
+    if (!ptx::mbar_wait(bar_b, 0)) {
+      set_device_error(kErrDecodeFullWait);
+      return;  // the only copy in flight is the one that never completed
+    }
+    if (kslice != 0) return;
+    // ---- acc_v += (P.L_a) . B_a for this warp's rows (K = window columns of agent a)
+    {
+      const int ag0 = row0 < p.rows ? row0 / p.G : -1;
+      const int ag1 = row1 < p.rows ? row1 / p.G : -1;
+#pragma unroll
+      for (int ks = 0; ks < NLT / 2; ++ks) {
+        if (ks * 16 >= win) break;  // warp-uniform
+        for (int a = a_lo; a <= a_hi; ++a) {
+          const int blk = a * p.l_agent_stride - c_lo;          // agent a's first window column
+          if (ks * 16 < blk || ks * 16 >= blk + p.r) continue;  // this k-step is not agent a's
+          const int kb = ks * 16 - blk;                          // first row of B_a for this k-step
+          const bool own0 = (ag0 == a), own1 = (ag1 == a);
+          uint32_t ah[4], al[4];
+          ah[0] = pack_hi_lo(own0 ? acc_l[2 * ks][0] : 0.f, own0 ? acc_l[2 * ks][1] : 0.f, al[0]);
+          ah[1] = pack_hi_lo(own1 ? acc_l[2 * ks][2] : 0.f, own1 ? acc_l[2 * ks][3] : 0.f, al[1]);
+          ah[2] = pack_hi_lo(own0 ? acc_l[2 * ks + 1][0] : 0.f, own0 ? acc_l[2 * ks + 1][1] : 0.f, al[2]);
+          ah[3] = pack_hi_lo(own1 ? acc_l[2 * ks + 1][2] : 0.f, own1 ? acc_l[2 * ks + 1][3] : 0.f, al[3]);
+          const int mi = lane >> 3, ri = lane & 7;
+          const int rr = (mi & 1) * 8 + ri;                 // row within the 16-row box
+          const int kc = (a * p.r + kb) >> 4;               // 16-row box index
+          const uint32_t bbox = ptx::smem_u32(bs) + kc * (D / 64) * 2048 + rr * 128;
+#pragma unroll
+          for (int dp = 0; dp < D / 16; ++dp) {
+            const int c16 = dp * 2 + (mi >> 1);
+            uint32_t bb[4];
+            ptx::ldsm_x4_t(bbox + (c16 >> 3) * 2048 + (swz_chunk(c16 & 7, rr, 128) << 4), bb);
+            ptx::mma_bf16(acc_v[2 * dp], ah, bb[0], bb[1]);
+            ptx::mma_bf16(acc_v[2 * dp + 1], ah, bb[2], bb[3]);
+            ptx::mma_bf16(acc_v[2 * dp], al, bb[0], bb[1]);
+            ptx::mma_bf16(acc_v[2 * dp + 1], al, bb[2], bb[3]);
+          }
+        }
+      }
+    }
+    // ---- O = (P.V_base + (P.L_a).B_a) / l, straight from the fragments
+    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int row = h2 ? row1 : row0;
+      if (row >= p.rows) continue;
+      const int a = row / p.G, j = head * p.G + row % p.G;
+      float *o = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D;
+      const float inv = h2 ? inv1 : inv0;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2 *>(o + i * 8 + 2 * t4) =
+            make_float2(acc_v[i][2 * h2] * inv, acc_v[i][2 * h2 + 1] * inv);
+    }
     return;
   }
 
-  // ---- single unit: O = (P.V_base + (P.L_a).B_a) / l
-  for (int e = threadIdx.x; e < p.rows * D; e += kNT) {
-    const int row = e / D, c = e % D;
-    const int a = row / p.G, j = head * p.G + row % p.G;
-    const float ls = ml[row];
-    p.O[(((int64_t)q * p.A + a) * p.hq + j) * D + c] = ls > 0.f ? mv[e] / ls : 0.f;
+  // ---- several units: publish this unit's partial straight from the
+  //      fragments: [rows][D + r] (P.V_base | own agent's P.L_a) | m[rows] | l[rows]
+  if (kslice != 0) return;
+  {
+    const int W = D + p.r;
+    float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int row = h2 ? row1 : row0;
+      if (row >= p.rows) continue;
+      float *drow = dst + row * W;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2 *>(drow + i * 8 + 2 * t4) = make_float2(acc_v[i][2 * h2], acc_v[i][2 * h2 + 1]);
+      const int blk = (row / p.G - a_lo) * p.l_agent_stride;  // own block's first window column
+#pragma unroll
+      for (int i = 0; i < NLT; ++i) {
+        const int c = i * 8 + 2 * t4;
+        if (c >= blk && c + 1 < blk + p.r)
+          *reinterpret_cast<float2 *>(drow + D + c - blk) = make_float2(acc_l[i][2 * h2], acc_l[i][2 * h2 + 1]);
+      }
+      if (t4 == 0) {
+        dst[p.rows * W + row] = h2 ? m1 : m0;
+        dst[p.rows * W + p.rows + row] = h2 ? l1 : l0;
+      }
+    }
   }
 }
 
@@ -619,6 +635,8 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
         *reinterpret_cast<const uint4 *>(p.B + ((int64_t)(a * r + k) * p.hkv + head) * D + c8 * 8);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the next decode may be scheduled now (it waits for this grid before reading)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int ug0, nu;
   if (p.single_len >= 0) {
     ug0 = 0;
@@ -823,12 +841,6 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
 
 inline bool decode_tc_shape_supported(const fla_attn_dims &d) { return decode_tc_plan(d).ok; }
 
-inline int device_sm_count() {
-  int dev = 0, n = 148;
-  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 148;
-}
-
 // Tokens per work unit.  Single request: split every kv head's context into
 // floor(SMs / hkv) units so one wave covers the GPU.  Several requests: aim at
 // about four units per SM so the block scheduler balances ragged lengths.
@@ -891,12 +903,28 @@ inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, con
                                 const CUtensorMap &mL, const CUtensorMap &mB, const dec::Params &prm, unsigned grid,
                                 bool need_merge, cudaStream_t s) {
   auto kern = dec::decode_tc_kernel<D, MT, TG, NLT, SG>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);
+  cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), pl.smem_bytes);
   if (e != cudaSuccess) {
     decode_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;
   }
-  kern<<<grid, dec::Cfg<D, MT, TG, NLT, SG>::kThreads, pl.smem_bytes, s>>>(mK, mV, mL, mB, prm);
+  {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(dec::Cfg<D, MT, TG, NLT, SG>::kThreads);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, kern, mK, mV, mL, mB, prm);
+    if (e != cudaSuccess) {
+      decode_tc_err() = cudaGetErrorString(e);
+      return FLA_ERR_CUDA;
+    }
+  }
   if (!need_merge) return FLA_OK;
   dec::MergeParams mp{};
   mp.partials = prm.partials;
@@ -912,8 +940,7 @@ inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, con
   // this row's B slice plus the cross-warp reduction buffer
   cfg.dynamicSmemBytes = (size_t)prm.r * D * 2 + 4 * 32 * (D / 32 + 4) * 4;
   if (cfg.dynamicSmemBytes > 48 * 1024) {
-    e = cudaFuncSetAttribute(dec::decode_merge_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)cfg.dynamicSmemBytes);
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(dec::decode_merge_kernel<D>), (int)cfg.dynamicSmemBytes);
     if (e != cudaSuccess) {
       decode_tc_err() = cudaGetErrorString(e);
       return FLA_ERR_CUDA;

@@ -5,6 +5,9 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace fla {
 
 // Device error word of this library image.  A kernel whose bounded wait runs
@@ -47,6 +50,54 @@ template <>
 __device__ __forceinline__ float from_f32<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+// ---------------------------------------------------------------------------
+// Host-side caches of per-device facts, so a launch does no redundant driver
+// calls: the SM count and each kernel's raised dynamic shared-memory limit.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+
+inline int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  return dev;
+}
+
+inline int device_sm_count() {
+  static std::atomic<int> cache[kMaxDevices];  // 0 = not looked up yet
+  const int dev = current_device();
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  n = 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) once per (kernel, device,
+// size): later launches of the same kernel with no more shared memory skip it.
+inline cudaError_t ensure_dynamic_smem(const void *kernel, int bytes) {
+  struct Entry {
+    const void *fn;
+    int dev, bytes;
+  };
+  static std::mutex mu;
+  static Entry entries[256];
+  static int n_entries = 0;
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n_entries; ++i)
+    if (entries[i].fn == kernel && entries[i].dev == dev && entries[i].bytes >= bytes) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) return e;
+  for (int i = 0; i < n_entries; ++i)
+    if (entries[i].fn == kernel && entries[i].dev == dev) {
+      entries[i].bytes = bytes;
+      return cudaSuccess;
+    }
+  if (n_entries < 256) entries[n_entries++] = Entry{kernel, dev, bytes};
+  return cudaSuccess;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -491,7 +491,7 @@ inline fla_status prefill_tc_launch(const fla_attn_dims &d, float scale, const v
 #define FLA_PRE_CASE(DD, MM)                                                                              \
   if (pl.D == DD && pl.MT == MM) {                                                                        \
     auto kern = pre::prefill_mma_kernel<DD, MM, 8>;                                                       \
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, pl.smem_bytes);           \
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), pl.smem_bytes);                        \
     if (e == cudaSuccess) kern<<<(unsigned)grid64, MM * 32, pl.smem_bytes, s>>>(mK, mV, mL, mB, prm);     \
     if (e != cudaSuccess) {                                                                               \
       prefill_tc_err() = cudaGetErrorString(e);                                                           \

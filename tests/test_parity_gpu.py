@@ -155,6 +155,18 @@ def test_decode_tensor_and_simt_agree_and_are_deterministic():
     check_attn(O1, O3.double().cpu().numpy(), what="tensor vs simt")
 
 
+def test_prepared_decode_matches_the_function():
+    w = small_workload(3, 32, 8, 128, 16)
+    x = to_dev(make_decode_inputs(w, seed=13, lengths=[5000, 70, 1]))
+    fla = _fla()
+    O1 = fla.flash_lora_attn_decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"], rank=16)
+    call = fla.PreparedDecode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"], rank=16)
+    for _ in range(2):
+        O2 = call()
+        torch.cuda.synchronize()
+        assert torch.equal(O1, O2)
+
+
 def test_decode_output_guard_bands():
     """Writes stay inside O: canaries around the output are untouched."""
     w = small_workload(3, 32, 8, 128, 16)
