@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_lib", "libflashlora.so")
 
 FLA_OK = 0
 FLA_F32, FLA_BF16 = 0, 1
-KERNELS = {"auto": 0, "simt": 1, "tensor": 2}
+KERNELS = {"auto": 0, "simt": 1, "tensor": 2, "mma": 3, "tcgen05": 4}
 STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "FLA_ERR_WORKSPACE",
           4: "FLA_ERR_CUDA", 5: "FLA_ERR_DEVICE_TIMEOUT"}
 

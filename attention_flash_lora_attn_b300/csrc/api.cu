@@ -20,6 +20,7 @@
 #include "decode_tc.cuh"
 #include "build_tc.cuh"
 #include "prefill_mma.cuh"
+#include "prefill_tc.cuh"
 
 namespace {
 
@@ -59,7 +60,7 @@ fla_status check_dims(const fla_attn_dims *d, float *scale) {
     return fail(FLA_ERR_UNSUPPORTED, "rank %d: must be in [1, 256]", d->rank);
   if (d->dtype != FLA_F32 && d->dtype != FLA_BF16)
     return fail(FLA_ERR_INVALID_ARG, "dtype %d is not FLA_F32 or FLA_BF16", d->dtype);
-  if (d->kernel < FLA_KERNEL_AUTO || d->kernel > FLA_KERNEL_TENSOR)
+  if (d->kernel < FLA_KERNEL_AUTO || d->kernel > FLA_KERNEL_TCGEN05)
     return fail(FLA_ERR_INVALID_ARG, "kernel %d is not a fla_kernel", d->kernel);
   if (d->l_agent_stride < 0) return fail(FLA_ERR_INVALID_ARG, "l_agent_stride must be >= 0");
   const int64_t need = (int64_t)(d->n_agents - 1) * d->l_agent_stride + d->rank;
@@ -117,7 +118,7 @@ fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, 
   if (n_tokens < 0 || d_model < 1 || n_cols < 1)
     return fail(FLA_ERR_INVALID_ARG, "n_tokens must be >= 0, d_model and n_cols >= 1");
   if (dtype != FLA_F32 && dtype != FLA_BF16) return fail(FLA_ERR_INVALID_ARG, "bad dtype %d", dtype);
-  if (kernel < FLA_KERNEL_AUTO || kernel > FLA_KERNEL_TENSOR)
+  if (kernel < FLA_KERNEL_AUTO || kernel > FLA_KERNEL_TCGEN05)
     return fail(FLA_ERR_INVALID_ARG, "kernel %d is not a fla_kernel", kernel);
   if (ldx < d_model) return fail(FLA_ERR_INVALID_ARG, "ldx (%lld) < d_model (%d)", (long long)ldx, d_model);
   if (ldl < n_cols) return fail(FLA_ERR_INVALID_ARG, "ldl (%lld) < n_cols (%d)", (long long)ldl, n_cols);
@@ -125,8 +126,10 @@ fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, 
   if (!X || !A_t || !L) return fail(FLA_ERR_INVALID_ARG, "X, A_t and L must be non-NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+  if (kernel == FLA_KERNEL_MMA_SYNC)
+    return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build has no mma.sync kernel (use TENSOR or TCGEN05)");
   const bool tc_ok = fla::build_tc_supported(X, ldx, A_t, L, ldl, d_model, n_cols, dtype);
-  if (kernel == FLA_KERNEL_TENSOR && !tc_ok)
+  if ((kernel == FLA_KERNEL_TENSOR || kernel == FLA_KERNEL_TCGEN05) && !tc_ok)
     return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build: shape/alignment outside the tensor-core kernel "
                 "(needs bf16, d_model %% 64 == 0, n_cols %% 32 == 0, n_cols <= 512, 16-byte alignment)");
   if (tc_ok && kernel != FLA_KERNEL_SIMT) {
@@ -171,10 +174,12 @@ fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, cons
   if (total_tokens > INT32_MAX) return fail(FLA_ERR_UNSUPPORTED, "total_tokens must fit in int32 (offsets are int32)");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
+  if (dims->kernel == FLA_KERNEL_TCGEN05)
+    return fail(FLA_ERR_UNSUPPORTED, "decode has no tcgen05 kernel (its tensor-core kernel is mma.sync)");
   const bool shape_tc = fla::decode_tc_shape_supported(*dims);
   const bool align_tc = aligned16(Q) && aligned16(K_base) && aligned16(V_base) && aligned16(L) &&
                         aligned16(B) && aligned16(O) && (dims->l_row_stride % 8 == 0);
-  if (dims->kernel == FLA_KERNEL_TENSOR && !(shape_tc && align_tc))
+  if ((dims->kernel == FLA_KERNEL_TENSOR || dims->kernel == FLA_KERNEL_MMA_SYNC) && !(shape_tc && align_tc))
     return fail(FLA_ERR_UNSUPPORTED, "decode: shape/alignment outside the tensor-core kernel (%s)",
                 fla::decode_tc_limits());
   if (shape_tc && align_tc && dims->kernel != FLA_KERNEL_SIMT && total_tokens > 0) {
@@ -222,16 +227,28 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
   if (!Q || !K_base || !V_base || !L || !B || !O)
     return fail(FLA_ERR_INVALID_ARG, "Q, K_base, V_base, L, B and O must be non-NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const bool shape_tc = fla::prefill_tc_shape_supported(*dims);
   const bool align_tc = aligned16(Q) && aligned16(K_base) && aligned16(V_base) && aligned16(L) &&
                         aligned16(B) && aligned16(O) && (dims->l_row_stride % 8 == 0);
-  if (dims->kernel == FLA_KERNEL_TENSOR && !(shape_tc && align_tc))
-    return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside the tensor-core kernel (bf16; head_dim "
-                "64 or 128; rank %% 16 == 0 and <= 64; l_agent_stride 0 or rank; 16-byte alignment)");
-  if (shape_tc && align_tc && dims->kernel != FLA_KERNEL_SIMT) {
+  const bool tc5 = align_tc && fla::prefill_tcgen05_plan(*dims, chunk).ok;
+  const bool mma = align_tc && fla::prefill_tc_shape_supported(*dims);
+  const int32_t k = dims->kernel;
+  if (k == FLA_KERNEL_TCGEN05 && !tc5)
+    return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside the tcgen05 kernel (bf16; head_dim 64 or "
+                "128; A*hq/hkv <= 128; L width and A*rank <= 64; l_agent_stride 0 or rank; 16-byte alignment)");
+  if (k == FLA_KERNEL_MMA_SYNC && !mma)
+    return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside the mma.sync kernel (bf16; head_dim 64 or "
+                "128; rank %% 16 == 0 and <= 64; l_agent_stride 0 or rank; 16-byte alignment)");
+  if (k == FLA_KERNEL_TENSOR && !tc5 && !mma)
+    return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside both tensor-core kernels");
+  if (tc5 && (k == FLA_KERNEL_AUTO || k == FLA_KERNEL_TENSOR || k == FLA_KERNEL_TCGEN05)) {
+    st = fla::prefill_tcgen05_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, s);
+    if (st != FLA_OK) return fail(st, "prefill (tcgen05): %s", fla::prefill_tcgen05_last_error());
+    return check_launch("prefill (tcgen05)");
+  }
+  if (mma && k != FLA_KERNEL_SIMT) {
     st = fla::prefill_tc_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, s);
-    if (st != FLA_OK) return fail(st, "prefill (tensor): %s", fla::prefill_tc_last_error());
-    return check_launch("prefill (tensor)");
+    if (st != FLA_OK) return fail(st, "prefill (mma.sync): %s", fla::prefill_tc_last_error());
+    return check_launch("prefill (mma.sync)");
   }
   fla::SimtAttnParams p{};
   p.Q = Q; p.K = K_base; p.V = V_base; p.L = L; p.B = B; p.O = O; p.offsets = nullptr;

@@ -59,11 +59,21 @@ typedef enum {
 
 typedef enum { FLA_F32 = 0, FLA_BF16 = 1 } fla_dtype;
 
-/* Kernel family.  AUTO picks the tensor-core kernels where the shape allows
- * and the plain CUDA-core kernels otherwise.  SIMT forces the CUDA-core
- * kernels (every supported shape); TENSOR fails with FLA_ERR_UNSUPPORTED when
- * the shape is outside the tensor-core kernels' limits. */
-typedef enum { FLA_KERNEL_AUTO = 0, FLA_KERNEL_SIMT = 1, FLA_KERNEL_TENSOR = 2 } fla_kernel;
+/* Kernel family.  AUTO picks the fastest kernel the shape allows.  SIMT
+ * forces the CUDA-core kernels (every supported shape).  TENSOR uses a
+ * tensor-core kernel (tcgen05 where the operation has one and the shape fits,
+ * warp-level mma.sync otherwise) and fails with FLA_ERR_UNSUPPORTED when the
+ * shape is outside every tensor-core kernel's limits.  MMA_SYNC and TCGEN05
+ * pin the tensor-core generation: warp-level mma.sync (decode, prefill) or
+ * tcgen05 with TMEM accumulators (LR-cache build, prefill); an operation
+ * without a kernel of that generation returns FLA_ERR_UNSUPPORTED. */
+typedef enum {
+  FLA_KERNEL_AUTO = 0,
+  FLA_KERNEL_SIMT = 1,
+  FLA_KERNEL_TENSOR = 2,
+  FLA_KERNEL_MMA_SYNC = 3,
+  FLA_KERNEL_TCGEN05 = 4
+} fla_kernel;
 
 /* Shape of the attention problem (decode and prefill). */
 typedef struct {
@@ -162,6 +172,10 @@ FLA_API fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void 
  *   O        fp32 [A, chunk, hq, d]              (output)
  *   workspace as for decode, flash_lora_attn_prefill_workspace_size() bytes
  *            (may be 0 bytes / NULL when the size query returns 0).
+ * Kernels: tcgen05 (bf16; head_dim 64 or 128; A*(hq/hkv) <= 128; L width
+ * (r, or A*r) <= 64 and A*r <= 64; l_agent_stride 0 or r); mma.sync (bf16;
+ * head_dim 64 or 128; r % 16 == 0, r <= 64; l_agent_stride 0 or r); both need
+ * 16-byte aligned pointers and l_row_stride % 8 == 0.  SIMT covers the rest.
  * Errors as for decode.
  */
 FLA_API size_t flash_lora_attn_prefill_workspace_size(const fla_attn_dims *dims, int32_t chunk, int64_t n0);

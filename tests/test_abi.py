@@ -90,6 +90,26 @@ def test_tensor_kernel_refuses_unsupported_shapes(lib):
     assert _decode(lib, f) == 2
 
 
+def test_kernel_generation_selection_is_validated(lib):
+    p = ctypes.c_void_p(16)
+    d = _dims()
+    d.kernel = 5                                       # not a fla_kernel
+    assert _decode(lib, d) == 1
+    d.kernel = 4                                       # decode has no tcgen05 kernel
+    assert _decode(lib, d) == 2
+    assert "mma.sync" in lib.fla_last_error_message().decode()
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 1, 3, None) == 2   # build has no mma.sync kernel
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 0, 4, None) == 2   # fp32: outside tcgen05
+    # prefill: L width A*r = 96 > 64 is outside the tcgen05 kernel; refused before any launch
+    w = _dims(n_agents=3, rank=32, l_row_stride=96, l_agent_stride=32)
+    w.kernel = 4
+    assert lib.flash_lora_attn_prefill(ctypes.byref(w), p, p, p, p, p, 1, 20, p, None, 0, None) == 2
+    assert "tcgen05" in lib.fla_last_error_message().decode()
+    f = _dims(dtype_code=0)
+    f.kernel = 3
+    assert lib.flash_lora_attn_prefill(ctypes.byref(f), p, p, p, p, p, 1, 20, p, None, 0, None) == 2
+
+
 def test_empty_calls_are_noops(lib):
     assert _decode(lib, _dims(), n_req=0) == 0
     d = _dims()

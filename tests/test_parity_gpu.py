@@ -193,7 +193,7 @@ PREFILL_SMALL = [(1, 4, 4, 64, 8, 0, 5), (2, 8, 2, 128, 16, 37, 70), (4, 32, 8, 
                  (2, 4, 2, 128, 16, 0, 300)]
 
 
-@pytest.mark.parametrize("kernel", ["tensor", "simt"])
+@pytest.mark.parametrize("kernel", ["tensor", "mma", "simt"])
 @pytest.mark.parametrize("case", PREFILL_SMALL, ids=[f"p{i}" for i in range(len(PREFILL_SMALL))])
 def test_prefill_small(case, kernel):
     A, hq, hkv, d, r, n0, c = case
@@ -204,14 +204,51 @@ def test_prefill_small(case, kernel):
         O = _fla().flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], n0, rank=r,
                                            kernel=kernel)
     except _fla().FlaError as e:
-        if kernel == "tensor" and e.status == 2:
-            pytest.skip("shape outside the tensor-core prefill kernel")
+        if kernel in ("tensor", "mma") and e.status == 2:
+            pytest.skip("shape outside the tensor-core prefill kernels")
         raise
     ref = oracle.prefill(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], n0=n0, rank=r)
     check_attn(O, ref, what=f"prefill {case}")
 
 
-def test_prefill_llama8b_chunk_with_lr_build_sampled_rows():
+# (A, hq, hkv, d, r, n0, chunk, shared L, Q scale): shapes inside the tcgen05 kernel.  Ragged key
+# tails, partial 128-row blocks (A*G*QB < 128), L narrower than its 64-column box (shared L, small
+# A*r), head_dim 64, one key in total, and Q scaled up so the running max moves often (rescales).
+PREFILL_TC5 = [(4, 32, 8, 128, 16, 300, 129, False, 1.0), (4, 32, 8, 128, 16, 1000, 64, True, 1.0),
+               (3, 24, 8, 128, 16, 777, 50, False, 1.0), (2, 8, 8, 64, 32, 2000, 100, False, 4.0),
+               (1, 32, 8, 128, 64, 513, 300, False, 1.0), (8, 16, 8, 128, 8, 129, 17, False, 1.0),
+               (2, 2, 2, 128, 16, 0, 1, False, 1.0), (2, 16, 8, 128, 16, 3000, 40, False, 8.0)]
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma"])
+@pytest.mark.parametrize("case", PREFILL_TC5, ids=[f"t{i}" for i in range(len(PREFILL_TC5))])
+def test_prefill_tcgen05_shapes(case, kernel):
+    A, hq, hkv, d, r, n0, c, shared, qs = case
+    if kernel == "mma" and r % 16:
+        pytest.skip("the mma.sync prefill kernel needs rank % 16 == 0")
+    w = small_prefill(A, hq, hkv, d, r, n0, c)
+    x = make_prefill_inputs(w, seed=5, with_X=False)
+    x["Q"] = (x["Q"].float() * qs).to(x["Q"].dtype)  # power-of-two scale: exact in bf16
+    dx = to_dev(x)
+    L = dx["L"][:, :r] if shared else dx["L"]
+    O = _fla().flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], L, dx["B"], n0, rank=r,
+                                       l_agent_stride=0 if shared else r, kernel=kernel)
+    ref = oracle.prefill(x["Q"], x["K_base"], x["V_base"], x["L"][:, :r] if shared else x["L"], x["B"],
+                         n0=n0, rank=r, agent_stride=0 if shared else r)
+    check_attn(O, ref, what=f"prefill {kernel} {case}")
+
+
+def test_prefill_tcgen05_rejects_shapes_outside_it():
+    w = small_prefill(3, 16, 4, 128, 32, 1, 20)  # L width A*r = 96 > 64
+    dx = to_dev(make_prefill_inputs(w, seed=1, with_X=False))
+    with pytest.raises(_fla().FlaError) as ei:
+        _fla().flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], 1, rank=32,
+                                       kernel="tcgen05")
+    assert ei.value.status == 2
+
+
+@pytest.mark.parametrize("kernel", ["tcgen05", "mma"])
+def test_prefill_llama8b_chunk_with_lr_build_sampled_rows(kernel):
     """Build the chunk's LR rows on the GPU, then prefill; oracle on sampled positions."""
     w = WORKLOADS["llama8b_prefill"]
     x = make_prefill_inputs(w, seed=0)
@@ -220,11 +257,11 @@ def test_prefill_llama8b_chunk_with_lr_build_sampled_rows():
     fla = _fla()
     fla.lr_cache_build(dx["X"], A_t, dx["L"][w.n0:])
     O = fla.flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], w.n0,
-                                    rank=w.rank, kernel="tensor").cpu()
+                                    rank=w.rank, kernel=kernel).cpu()
     # oracle: its own LR rows for the chunk (fp64 product rounded to the bf16 storage type)
     L_ref = oracle.to_f64(x["L"]).copy()
     L_ref[w.n0:] = oracle.round_to_bf16(oracle.lr_cache_build(x["X"], x["A_cat"]))
-    pos = [0, 1, 255, 256, 510, 511]
+    pos = [0, 1, 7, 8, 255, 256, 510, 511]
     ref = oracle.prefill(x["Q"], x["K_base"], x["V_base"], L_ref, x["B"], n0=w.n0, rank=w.rank, positions=pos)
     check_attn(O[:, pos], ref[:, pos], what="llama8b prefill")
 
