@@ -18,6 +18,7 @@
 #include "fla_common.cuh"
 #include "simt_kernels.cuh"
 #include "decode_tc.cuh"
+#include "decode_t5.cuh"
 #include "build_tc.cuh"
 #include "prefill_mma.cuh"
 #include "prefill_tc.cuh"
@@ -153,8 +154,19 @@ size_t flash_lora_attn_decode_workspace_size(const fla_attn_dims *dims, int32_t 
   float scale = 0.f;
   if (check_dims(dims, &scale) != FLA_OK || n_req < 0 || total_tokens < 0) return 0;
   if (dims->kernel == FLA_KERNEL_SIMT) return 0;
-  if (!fla::decode_tc_shape_supported(*dims)) return 0;
-  return fla::decode_tc_workspace_bytes(*dims, n_req, total_tokens);
+  size_t need = 0;
+  if (dims->kernel != FLA_KERNEL_TCGEN05 && fla::decode_tc_shape_supported(*dims))
+    need = fla::decode_tc_workspace_bytes(*dims, n_req, total_tokens);
+  if (dims->kernel != FLA_KERNEL_MMA_SYNC && fla::decode_t5_shape_supported(*dims))
+    need = std::max(need, fla::decode_t5_workspace_bytes(*dims, n_req, total_tokens));
+  return need;
+}
+
+// The tcgen05 decode kernel is chosen over the mma.sync one for these shapes
+// (AUTO and TENSOR): groups of query rows large enough that the mma.sync
+// kernel becomes compute-latency bound.
+static bool prefer_tcgen05_decode(const fla_attn_dims &d) {
+  return d.n_agents * (d.hq / d.hkv) > 16;
 }
 
 fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, const void *K_base,
@@ -174,15 +186,36 @@ fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, cons
   if (total_tokens > INT32_MAX) return fail(FLA_ERR_UNSUPPORTED, "total_tokens must fit in int32 (offsets are int32)");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  if (dims->kernel == FLA_KERNEL_TCGEN05)
-    return fail(FLA_ERR_UNSUPPORTED, "decode has no tcgen05 kernel (its tensor-core kernel is mma.sync)");
-  const bool shape_tc = fla::decode_tc_shape_supported(*dims);
   const bool align_tc = aligned16(Q) && aligned16(K_base) && aligned16(V_base) && aligned16(L) &&
                         aligned16(B) && aligned16(O) && (dims->l_row_stride % 8 == 0);
-  if ((dims->kernel == FLA_KERNEL_TENSOR || dims->kernel == FLA_KERNEL_MMA_SYNC) && !(shape_tc && align_tc))
-    return fail(FLA_ERR_UNSUPPORTED, "decode: shape/alignment outside the tensor-core kernel (%s)",
+  const bool t5 = align_tc && fla::decode_t5_shape_supported(*dims);
+  const bool mma = align_tc && fla::decode_tc_shape_supported(*dims);
+  const int32_t k = dims->kernel;
+  if (k == FLA_KERNEL_TCGEN05 && !t5)
+    return fail(FLA_ERR_UNSUPPORTED, "decode: shape/alignment outside the tcgen05 kernel (bf16; head_dim 128; "
+                "n_agents*hq/hkv <= 64; rank <= 64; L width <= 512; l_agent_stride 0 or rank; 16-byte alignment)");
+  if (k == FLA_KERNEL_MMA_SYNC && !mma)
+    return fail(FLA_ERR_UNSUPPORTED, "decode: shape/alignment outside the mma.sync kernel (%s)",
                 fla::decode_tc_limits());
-  if (shape_tc && align_tc && dims->kernel != FLA_KERNEL_SIMT && total_tokens > 0) {
+  if (k == FLA_KERNEL_TENSOR && !mma && !t5)
+    return fail(FLA_ERR_UNSUPPORTED, "decode: shape/alignment outside both tensor-core kernels (%s)",
+                fla::decode_tc_limits());
+  const bool use_t5 = t5 && total_tokens > 0 &&
+                      (k == FLA_KERNEL_TCGEN05 ||
+                       ((k == FLA_KERNEL_AUTO || k == FLA_KERNEL_TENSOR) && (!mma || prefer_tcgen05_decode(*dims))));
+  if (use_t5) {
+    const size_t need = fla::decode_t5_workspace_bytes(*dims, n_req, total_tokens);
+    if (!workspace || workspace_bytes < need)
+      return fail(FLA_ERR_WORKSPACE, "decode: workspace of %zu bytes required, %zu given", need,
+                  workspace ? workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+      return fail(FLA_ERR_INVALID_ARG, "decode: workspace must be 256-byte aligned");
+    st = fla::decode_t5_launch(*dims, scale, Q, K_base, V_base, L, B, offsets, n_req, total_tokens, O, workspace, s);
+    if (st != FLA_OK) return fail(st, "decode (tcgen05): %s", fla::decode_tc_last_error());
+    return check_launch("decode (tcgen05)");
+  }
+  const bool shape_tc = mma;
+  if (shape_tc && k != FLA_KERNEL_SIMT && total_tokens > 0) {
     const size_t need = fla::decode_tc_workspace_bytes(*dims, n_req, total_tokens);
     if (need > 0 && (!workspace || workspace_bytes < need))
       return fail(FLA_ERR_WORKSPACE, "decode: workspace of %zu bytes required, %zu given", need,

@@ -115,6 +115,7 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     // ======================= MMA issuer =======================
     if (lane == 0) {
       const uint32_t idesc = ptx::idesc_bf16_f32(kBM, chunk);
+      const uint64_t d_smem = ptx::smem_desc_k128(ptx::smem_u32(smem));
       bool ok = true;
       for (int kt = 0; kt < n_k; ++kt) {
         const int s = kt % p.stages;
@@ -125,14 +126,14 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t sa = ptx::smem_u32(smem + s * stage_bytes);
+        const uint64_t da = ptx::desc_advance(d_smem, s * stage_bytes);
+        const uint64_t db = ptx::desc_advance(da, a_bytes);
 #pragma unroll
         for (int k16 = 0; k16 < kBK / 16; ++k16) {
-          const uint64_t adesc = ptx::smem_desc_k128(sa + k16 * 32);
-          for (int c = 0; c < p.n_chunks; ++c) {
-            const uint64_t bdesc = ptx::smem_desc_k128(sa + a_bytes + c * chunk * 128 + k16 * 32);
-            ptx::tc_mma_f16(tmem + c * chunk, adesc, bdesc, idesc, (kt > 0 || k16 > 0) ? 1u : 0u);
-          }
+          const uint32_t acc = (kt > 0 || k16 > 0) ? 1u : 0u;
+          for (int c = 0; c < p.n_chunks; ++c)
+            ptx::tc_mma_f16(tmem + c * chunk, ptx::desc_advance(da, k16 * 32),
+                            ptx::desc_advance(db, c * chunk * 128 + k16 * 32), idesc, acc);
         }
         ptx::tc_commit(empty0 + 8 * s);  // stage s is free once these MMAs have read it
       }

@@ -113,6 +113,58 @@ __device__ __forceinline__ uint32_t pack_hi_lo(float x0, float x1, uint32_t &lo)
   return (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
 }
 
+// Maps a global unit index to (request q, unit u of q, units of q, first
+// token, token count) in s_info[0..4]; returns whether the unit exists.  Run by
+// one whole warp: a prefix scan of the requests' unit counts, 32 at a time.
+// A request of length len has max(1, ceil(len / U)) units (an empty request
+// still gets one, which writes its zero output).
+__device__ __forceinline__ int map_unit(int unit_global, int U, int single_len, const int32_t *offsets, int n_req,
+                                        int *s_info) {
+  const int lane = threadIdx.x & 31;
+  int base = 0, found = 0;
+  if (single_len >= 0) {  // one request: its length is known, no scan
+    const int len = single_len;
+    const int nu = len > 0 ? (len + U - 1) / U : 1;
+    found = unit_global < nu;
+    if (found && lane == 0) {
+      s_info[0] = 0;
+      s_info[1] = unit_global;
+      s_info[2] = nu;
+      s_info[3] = unit_global * U;
+      s_info[4] = len > 0 ? min(U, len - unit_global * U) : 0;
+    }
+  }
+  for (int q0 = 0; q0 < n_req && !found; q0 += 32) {
+    const int q = q0 + lane;
+    int len = 0, nu = 0;
+    if (q < n_req) {
+      len = offsets[q + 1] - offsets[q];
+      nu = len > 0 ? (len + U - 1) / U : 1;
+    }
+    int incl = nu;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    const int excl = base + incl - nu;
+    const bool mine = (q < n_req) && unit_global >= excl && unit_global < excl + nu;
+    if (__ballot_sync(0xffffffffu, mine)) {
+      found = 1;
+      if (mine) {
+        const int u = unit_global - excl;
+        s_info[0] = q;
+        s_info[1] = u;
+        s_info[2] = nu;
+        s_info[3] = offsets[q] + u * U;
+        s_info[4] = len > 0 ? min(U, len - u * U) : 0;
+      }
+    }
+    base += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  return found;
+}
+
 template <int D, int MT, int TG, int NLT, int SG>
 __global__ void __launch_bounds__(Cfg<D, MT, TG, NLT, SG>::kThreads, 1)
 decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -144,48 +196,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
   // ---- map unit_global -> (request, unit) with a warp-parallel scan
   if (warp == 0) {
-    int base = 0, found = 0;
-    const int U = p.unit_tokens;
-    if (p.single_len >= 0) {  // one request: its length is known, no scan
-      const int len = p.single_len;
-      const int nu = len > 0 ? (len + U - 1) / U : 1;
-      found = unit_global < nu;
-      if (found && lane == 0) {
-        s_info[0] = 0;
-        s_info[1] = unit_global;
-        s_info[2] = nu;
-        s_info[3] = unit_global * U;
-        s_info[4] = len > 0 ? min(U, len - unit_global * U) : 0;
-      }
-    }
-    for (int q0 = 0; q0 < p.n_req && !found; q0 += 32) {
-      const int q = q0 + lane;
-      int len = 0, nu = 0;
-      if (q < p.n_req) {
-        len = p.offsets[q + 1] - p.offsets[q];
-        nu = len > 0 ? (len + U - 1) / U : 1;
-      }
-      int incl = nu;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int excl = base + incl - nu;
-      const bool mine = (q < p.n_req) && unit_global >= excl && unit_global < excl + nu;
-      if (__ballot_sync(0xffffffffu, mine)) {
-        found = 1;
-        if (mine) {
-          const int u = unit_global - excl;
-          s_info[0] = q;
-          s_info[1] = u;
-          s_info[2] = nu;
-          s_info[3] = p.offsets[q] + u * U;
-          s_info[4] = len > 0 ? min(U, len - u * U) : 0;
-        }
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
-    }
+    const int found = map_unit(unit_global, p.unit_tokens, p.single_len, p.offsets, p.n_req, s_info);
     if (lane == 0) {
       s_info[5] = found;
       s_flag[0] = 0;
@@ -614,6 +625,7 @@ struct MergeParams {
   const __nv_bfloat16 *B;
   float *O;
   int32_t n_req, A, hq, hkv, G, r, rows, part_stride, unit_tokens, single_len;
+  int32_t merge_single;  // 1: single-unit pairs have a partial too (finish them here)
 };
 
 template <int D>
@@ -646,7 +658,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) 
     ug0 = info.x;
     nu = info.y;
   }
-  if (nu <= 1) return;  // written directly by the decode kernel (uniform over the CTA)
+  if (nu <= 1 && !p.merge_single) return;  // written directly by the decode kernel (uniform over the CTA)
   const int W = D + r;
   const int64_t ustride = (int64_t)p.hkv * p.part_stride;
   const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;

@@ -18,6 +18,7 @@ enum DeviceErrorCode : uint32_t {
   kErrNone = 0,
   kErrDecodeFullWait = 0x101,   // decode consumer: stage never filled
   kErrDecodeEmptyWait = 0x102,  // decode producer: stage never released
+  kErrDecodeT5Wait = 0x103,     // tcgen05 decode: any pipeline wait
   kErrBuildFullWait = 0x201,    // LR build MMA warp: operands never landed
   kErrBuildEmptyWait = 0x202,   // LR build producer: stage never released
   kErrBuildAccWait = 0x203,     // LR build epilogue: accumulator never committed

@@ -26,9 +26,9 @@
 // (P.L_a).B_a: A = the OL row of each query restricted to its own agent's
 // columns (bf16 high + low parts, K = 2*A*r), B = [B_cat; B_cat] of the head.
 //
-// Warp roles: warp 0 lane 0 issues TMA (K ring, V|L ring, B); warp 1 owns the
-// TMEM allocation and lane 0 issues every MMA; warps 2..5 run the softmax and
-// the epilogue.  Every wait is bounded; on a timeout the kernel records the
+// Warp roles: warp 0 lane 0 issues the K ring's TMA copies (then B), warp 6
+// lane 0 the V|L ring's; warp 1 owns the TMEM allocation and lane 0 issues
+// every MMA; warps 2..5 run the softmax and the epilogue.  Every wait is bounded; on a timeout the kernel records the
 // error, drains its own copies and MMAs, frees TMEM and returns.
 #pragma once
 
@@ -44,7 +44,8 @@ namespace ptc {
 
 constexpr int kT = 128;          // keys per tile
 constexpr int kM = 128;          // query rows per CTA (MMA M)
-constexpr int kThreads = 192;    // 6 warps
+constexpr int kThreads = 224;    // 7 warps
+constexpr int kVWarp = 6;        // the V|L producer warp
 constexpr int kBoxBytes = 128 * 128;  // one 64-column box of a 128-row tile
 constexpr uint32_t kColS0 = 0, kColS1 = 128, kColO = 256, kColP = 448;  // TMEM columns
 constexpr float kRescaleLog2 = 8.f;  // raise the running max only past 2^8
@@ -60,19 +61,8 @@ struct Params {
   float scale_log2;
 };
 
-// Bounded wait that also gives up once another role has flagged an abort.
 __device__ __forceinline__ bool wait_ab(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      set_device_error(kErrPrefillWait);
-      *abort_flag = 1;
-      return false;
-    }
-  }
+  return ptx::mbar_wait_or_abort(bar, parity, abort_flag, kErrPrefillWait);
 }
 
 template <int D>
@@ -158,40 +148,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
   const uint32_t tmem = s_tmem;
   bool ok = true;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == 0 || warp == kVWarp) {
+    // ------------------------------------------------------------ TMA producers:
+    // warp 0 streams the K ring (then B_cat), warp kVWarp the V|L ring, so
+    // neither ring waits behind the other's free slots
     int k_issued = 0, v_issued = 0;
     bool b_issued = false;
-    if (lane == 0) {
+    if (lane == 0 && warp == 0) {
       ptx::prefetch_tmap(&tmK);
-      ptx::prefetch_tmap(&tmV);
-      ptx::prefetch_tmap(&tmL);
       ptx::prefetch_tmap(&tmB);
-      auto load_k = [&](int j) -> bool {
+      for (int j = 0; ok && j < n; ++j) {
         const int st = j % p.nk;
-        if (j >= p.nk && !wait_ab(ke(st), ((j / p.nk) - 1) & 1, &s_abort)) return false;
+        if (j >= p.nk && !wait_ab(ke(st), ((j / p.nk) - 1) & 1, &s_abort)) {
+          ok = false;
+          break;
+        }
         ptx::mbar_arrive_expect_tx(kf(st), kKBytes);
         const uint32_t dst = ptx::smem_u32(k_s + st * kKBytes);
 #pragma unroll
-        for (int b = 0; b < D / 64; ++b) ptx::tma_load_3d(dst + b * kBoxBytes, &tmK, b * 64, head, j * kT, kf(st));
+        for (int b = 0; b < D / 64; ++b)
+          ptx::tma_load_3d(dst + b * kBoxBytes, &tmK, b * 64, head, j * kT, kf(st));
         k_issued = j + 1;
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        const int st = j % p.nv;
-        if (j >= p.nv && !wait_ab(ve(st), ((j / p.nv) - 1) & 1, &s_abort)) return false;
-        ptx::mbar_arrive_expect_tx(vf(st), kVLBytes);
-        const uint32_t dst = ptx::smem_u32(vl_s + st * kVLBytes);
-#pragma unroll
-        for (int b = 0; b < D / 64; ++b) ptx::tma_load_3d(dst + b * kBoxBytes, &tmV, b * 64, head, j * kT, vf(st));
-        ptx::tma_load_2d(dst + (D / 64) * kBoxBytes, &tmL, 0, j * kT, vf(st));
-        v_issued = j + 1;
-        return true;
-      };
-      ok = load_k(0);
-      for (int j = 0; ok && j < n; ++j) {
-        if (j + 1 < n) ok = load_k(j + 1);
-        if (ok) ok = load_v(j);
       }
       // B_cat rows of this head for the epilogue GEMM, into the K ring once
       // the last S MMA (hence every S MMA) has finished with it
@@ -205,10 +182,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       }
       if (!ok) s_abort = 1;
     }
+    if (lane == 0 && warp == kVWarp) {
+      ptx::prefetch_tmap(&tmV);
+      ptx::prefetch_tmap(&tmL);
+      for (int j = 0; ok && j < n; ++j) {
+        const int st = j % p.nv;
+        if (j >= p.nv && !wait_ab(ve(st), ((j / p.nv) - 1) & 1, &s_abort)) {
+          ok = false;
+          break;
+        }
+        ptx::mbar_arrive_expect_tx(vf(st), kVLBytes);
+        const uint32_t dst = ptx::smem_u32(vl_s + st * kVLBytes);
+#pragma unroll
+        for (int b = 0; b < D / 64; ++b)
+          ptx::tma_load_3d(dst + b * kBoxBytes, &tmV, b * 64, head, j * kT, vf(st));
+        ptx::tma_load_2d(dst + (D / 64) * kBoxBytes, &tmL, 0, j * kT, vf(st));
+        v_issued = j + 1;
+      }
+      if (!ok) s_abort = 1;
+    }
     ptx::tc_fence_before();
     __syncthreads();
     if (s_abort && lane == 0) {
-      // wait for this CTA's own copies still in flight: the latest load of each stage
+      // wait for this warp's own copies still in flight: the latest load of each stage
       for (int j = max(0, k_issued - p.nk); j < k_issued; ++j) ptx::mbar_wait(kf(j % p.nk), (j / p.nk) & 1);
       for (int j = max(0, v_issued - p.nv); j < v_issued; ++j) ptx::mbar_wait(vf(j % p.nv), (j / p.nv) & 1);
       if (b_issued) ptx::mbar_wait(bfull, 0);
@@ -220,17 +216,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       const uint32_t idesc_s = ptx::idesc_bf16_f32(kM, kT);
       const uint32_t idesc_pv = ptx::idesc_bf16_f32(kM, D + 64) | (1u << 16);  // B (V|L) MN-major
       const uint32_t idesc_ep = ptx::idesc_bf16_f32(kM, D) | (1u << 16);       // B (B_cat) MN-major
-      const uint32_t qa = ptx::smem_u32(q_s);
+      const uint64_t d_q = ptx::smem_desc_k128(ptx::smem_u32(q_s));
+      const uint64_t d_k = ptx::smem_desc_k128(ptx::smem_u32(k_s));
+      const uint64_t d_vl = ptx::smem_desc_mn128(ptx::smem_u32(vl_s), kBoxBytes);
       auto issue_s = [&](int j) -> bool {
         const int st = j % p.nk, b = j & 1;
         if (!wait_ab(kf(st), (j / p.nk) & 1, &s_abort)) return false;
         if (j >= 2 && !wait_ab(sfree(b), ((j >> 1) - 1) & 1, &s_abort)) return false;
         ptx::tc_fence_after();
-        const uint32_t kb = ptx::smem_u32(k_s + st * kKBytes);
+        const uint64_t dk = ptx::desc_advance(d_k, st * kKBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = (ks >> 2) * kBoxBytes + (ks & 3) * 32;
-          ptx::tc_mma_f16(tmem + (b ? kColS1 : kColS0), ptx::smem_desc_k128(qa + off), ptx::smem_desc_k128(kb + off),
+          ptx::tc_mma_f16(tmem + (b ? kColS1 : kColS0), ptx::desc_advance(d_q, off), ptx::desc_advance(dk, off),
                           idesc_s, ks > 0 ? 1u : 0u);
         }
         issued_any = true;
@@ -243,11 +241,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (!wait_ab(pfull, j & 1, &s_abort)) return false;
         if (!wait_ab(vf(st), (j / p.nv) & 1, &s_abort)) return false;
         ptx::tc_fence_after();
-        const uint32_t vb = ptx::smem_u32(vl_s + st * kVLBytes);
+        const uint64_t dv = ptx::desc_advance(d_vl, st * kVLBytes);
 #pragma unroll
         for (int ks = 0; ks < kT / 16; ++ks)
-          ptx::tc_mma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, ptx::smem_desc_mn128(vb + ks * 16 * 128, kBoxBytes),
-                             idesc_pv, (j > 0 || ks > 0) ? 1u : 0u);
+          ptx::tc_mma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, ptx::desc_advance(dv, ks * 16 * 128), idesc_pv,
+                             (j > 0 || ks > 0) ? 1u : 0u);
         ptx::tc_commit(ve(st));
         ptx::tc_commit(pvdone);
         return true;
@@ -262,11 +260,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       if (ok) ok = wait_ab(bfull, 0, &s_abort);
       if (ok) {
         ptx::tc_fence_after();
-        const uint32_t bb = ptx::smem_u32(k_s);
+        const uint64_t dbb = ptx::smem_desc_mn128(ptx::smem_u32(k_s), 64 * 128);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          ptx::tc_mma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, ptx::smem_desc_mn128(bb + (ks & 3) * 16 * 128, 64 * 128),
-                             idesc_ep, 1u);
+          ptx::tc_mma_f16_ts(tmem + kColO, tmem + kColP + ks * 8, ptx::desc_advance(dbb, (ks & 3) * 16 * 128), idesc_ep,
+                             1u);
         ptx::tc_commit(pvdone);
       }
       if (!ok) s_abort = 1;
@@ -277,7 +275,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       ptx::tc_commit(drain);  // completes once every MMA this thread issued has finished
       ptx::mbar_wait(drain, 0);
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ------------------------------------------------------------ softmax + epilogue
     const int q = warp & 3;
     const int row = q * 32 + lane;
@@ -300,65 +298,114 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         break;
       }
       ptx::tc_fence_after();
+      const uint32_t s_col = tmem + lane_base + (b ? kColS1 : kColS0);
       uint32_t sv[kT];
-#pragma unroll
-      for (int c = 0; c < kT / 32; ++c)
-        ptx::tmem_ld32(tmem + lane_base + (b ? kColS1 : kColS0) + c * 32,
-                       *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
-      ptx::tmem_ld_wait();
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(sfree(b));
+      auto sv32 = [&](int c) -> uint32_t(&)[32] { return *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]); };
       const int64_t tile0 = (int64_t)j * kT;
-      if (tile0 + kT > causal_from) {
-        const int64_t rel = lim - tile0;  // keys i >= rel of this tile are masked
-#pragma unroll
-        for (int i = 0; i < kT; ++i)
-          if (i >= rel) sv[i] = 0xff800000u;  // -inf
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < kT; ++i) mx = fmaxf(mx, __uint_as_float(sv[i]));
-      const float mt = mx * sl2;
-      bool need = false;
-      if (j == 0) m_used = mt;
-      else need = mt > m_used + kRescaleLog2;
-      bool waited = false;
-      if (__any_sync(0xffffffffu, need)) {
-        // rescale O and OL of the rows whose max moved: PV_{j-1} must have finished
-        if (!__all_sync(0xffffffffu, wait_ab(pvdone, (j - 1) & 1, &s_abort))) {
-          ok = false;
-          break;
-        }
-        waited = true;
-        ptx::tc_fence_after();
-        const float f = need ? ptx::ex2(m_used - mt) : 1.f;
-        if (need) {
-          m_used = mt;
-          l *= f;
-        }
-#pragma unroll
-        for (int c = 0; c < (D + 64) / 32; ++c) {
-          uint32_t ov[32];
-          ptx::tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
-          ptx::tmem_st32(tmem + lane_base + kColO + c * 32, ov);
-        }
-        ptx::tmem_st_wait();
-      }
-      const float moff = (m_used == -INFINITY) ? 0.f : m_used;
+      const bool masked = tile0 + kT > causal_from;
+      const int64_t rel = lim - tile0;  // keys i >= rel of this tile are masked for this row
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float rsum[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t pk[kT / 2];
-      float rs = 0.f;
+      // mask + running column max of keys [h*64, h*64 + 64)
+      auto mask_max = [&](int h) {
+        if (masked) {  // only the tiles that reach the chunk
 #pragma unroll
-      for (int i = 0; i < kT / 2; ++i) {
-        const float e0 = ptx::ex2(fmaf(__uint_as_float(sv[2 * i]), sl2, -moff));
-        const float e1 = ptx::ex2(fmaf(__uint_as_float(sv[2 * i + 1]), sl2, -moff));
-        rs += e0 + e1;
-        pk[i] = ptx::pack_bf16(e0, e1);
+          for (int i = 0; i < 64; ++i)
+            if (64 * h + i >= rel) sv[64 * h + i] = 0xff800000u;  // -inf
+        }
+#pragma unroll
+        for (int i = 0; i < 64; ++i) mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sv[64 * h + i]));
+      };
+      // P = exp2(S*scale - moff) for keys [h*64, h*64 + 64), packed bf16 pairs
+      auto exps = [&](int h, float moff) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float e0 = ptx::ex2(fmaf(__uint_as_float(sv[64 * h + 2 * i]), sl2, -moff));
+          const float e1 = ptx::ex2(fmaf(__uint_as_float(sv[64 * h + 2 * i + 1]), sl2, -moff));
+          rsum[i & 3] += e0;
+          rsum[(i + 2) & 3] += e1;
+          pk[32 * h + i] = ptx::pack_bf16(e0, e1);
+        }
+      };
+      auto load_half = [&](int h) {
+        ptx::tmem_ld32(s_col + 64 * h, sv32(2 * h));
+        ptx::tmem_ld32(s_col + 64 * h + 32, sv32(2 * h + 1));
+      };
+      auto land_half = [&](int h) {
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(sv32(2 * h));
+        ptx::reg_fence32(sv32(2 * h + 1));
+      };
+      auto release_s = [&]() {
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sfree(b));
+      };
+      bool waited = false;
+      load_half(0);
+      land_half(0);
+      load_half(1);  // the second half lands while the first is processed
+      if (j == 0) {
+        mask_max(0);
+        land_half(1);
+        release_s();
+        mask_max(1);
+        m_used = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const float moff = (m_used == -INFINITY) ? 0.f : m_used;
+        exps(0, moff);
+        exps(1, moff);
+      } else {
+        // past the first tile the exponentials use the running max
+        // speculatively: it only moves when this tile's max exceeds it by 2^8
+        mask_max(0);
+        exps(0, m_used);
+        land_half(1);
+        release_s();
+        mask_max(1);
+        exps(1, m_used);
+        const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl2;
+        const bool need = mt > m_used + kRescaleLog2;
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale O and OL of the rows whose max moved: PV_{j-1} must have finished
+          if (!__all_sync(0xffffffffu, wait_ab(pvdone, (j - 1) & 1, &s_abort))) {
+            ok = false;
+            break;
+          }
+          waited = true;
+          ptx::tc_fence_after();
+          const float f = need ? ptx::ex2(m_used - mt) : 1.f;
+          if (need) {
+            m_used = mt;
+            l *= f;
+          }
+#pragma unroll
+          for (int c = 0; c < (D + 64) / 32; ++c) {
+            uint32_t ov[32];
+            ptx::tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
+            ptx::tmem_ld_wait();
+            ptx::reg_fence32(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f);
+            ptx::tmem_st32(tmem + lane_base + kColO + c * 32, ov);
+          }
+          ptx::tmem_st_wait();
+          // recompute P with the new max from S_j, still intact in TMEM: the
+          // MMA thread issues S_{j+2} into this buffer only after PV_j, which
+          // waits for P_j
+          load_half(0);
+          load_half(1);
+          land_half(1);
+          ptx::reg_fence32(sv32(0));
+          ptx::reg_fence32(sv32(1));
+          rsum[0] = rsum[1] = rsum[2] = rsum[3] = 0.f;
+          mask_max(0);
+          mask_max(1);
+          exps(0, m_used);
+          exps(1, m_used);
+        }
       }
-      l += rs;
+      l += (rsum[0] + rsum[1]) + (rsum[2] + rsum[3]);
       if (j > 0 && !waited) {
         // the P buffer is free once PV_{j-1} has finished reading it
         if (!__all_sync(0xffffffffu, wait_ab(pvdone, (j - 1) & 1, &s_abort))) {
@@ -382,6 +429,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
       ptx::tmem_ld32(tmem + lane_base + kColOL, *reinterpret_cast<uint32_t(*)[32]>(&olr[0]));
       ptx::tmem_ld32(tmem + lane_base + kColOL + 32, *reinterpret_cast<uint32_t(*)[32]>(&olr[32]));
       ptx::tmem_ld_wait();
+      ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&olr[0]));
+      ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&olr[32]));
       // own-row staging in the (now idle) V|L ring, [column][row]: lets the
       // agent's window be indexed at run time
       float *olT = reinterpret_cast<float *>(vl_s);
@@ -420,6 +469,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         uint32_t ov[32];
         ptx::tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
         ptx::tmem_ld_wait();
+        ptx::reg_fence32(ov);
         if (orow) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)

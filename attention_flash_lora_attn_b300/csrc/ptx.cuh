@@ -59,6 +59,24 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
 }
 
+// Bounded wait that also gives up once another role of the CTA has raised
+// *abort_flag; on its own timeout it records `err` in the device error word
+// and raises the flag.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                   uint32_t err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_device_error(err);
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+
 // ----------------------------------------------------------------- TMA loads
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -176,6 +194,13 @@ __device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t box
   return d;
 }
 
+// A matrix descriptor whose start address is `bytes` (a multiple of 16)
+// further on.  The start-address field is the low 14 bits (address >> 4) and
+// every shared-memory address of a CTA is below 256 KB, so the addition never
+// carries into the other fields: one 64-bit add per MMA instead of rebuilding
+// the descriptor keeps the single issuing thread ahead of the tensor core.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 D, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                 // D format: f32
@@ -224,6 +249,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
       : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties 32 registers written by tcgen05.ld to a point after tcgen05.wait::ld:
+// the compiler cannot move a use of them above this (empty) statement.
+__device__ __forceinline__ void reg_fence32(uint32_t (&v)[32]) {
+  asm volatile(""
+               : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                 "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                 "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                 "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                 "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
+}
 
 // Store 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane per thread).
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {

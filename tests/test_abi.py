@@ -95,9 +95,10 @@ def test_kernel_generation_selection_is_validated(lib):
     d = _dims()
     d.kernel = 5                                       # not a fla_kernel
     assert _decode(lib, d) == 1
-    d.kernel = 4                                       # decode has no tcgen05 kernel
-    assert _decode(lib, d) == 2
-    assert "mma.sync" in lib.fla_last_error_message().decode()
+    h = _dims(head_dim=64)
+    h.kernel = 4                                       # the tcgen05 decode kernel needs head_dim 128
+    assert _decode(lib, h) == 2
+    assert "tcgen05" in lib.fla_last_error_message().decode()
     assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 1, 3, None) == 2   # build has no mma.sync kernel
     assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 0, 4, None) == 2   # fp32: outside tcgen05
     # prefill: L width A*r = 96 > 64 is outside the tcgen05 kernel; refused before any launch

@@ -75,7 +75,7 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("kernel", ["tensor", "simt"])
+@pytest.mark.parametrize("kernel", ["tensor", "mma", "tcgen05", "simt"])
 @pytest.mark.parametrize("case", SMALL, ids=[f"s{i}" for i in range(len(SMALL))])
 def test_decode_small(case, kernel):
     lengths, A, hq, hkv, d, r, shared = case
@@ -84,15 +84,15 @@ def test_decode_small(case, kernel):
     try:
         O = run_decode(x, r, kernel, shared)
     except _fla().FlaError as e:
-        if kernel == "tensor" and e.status == 2:
-            pytest.skip("shape outside the tensor-core decode kernel")
+        if kernel in ("tensor", "mma", "tcgen05") and e.status == 2:
+            pytest.skip("shape outside this tensor-core decode kernel")
         raise
     ref = oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"].numpy(), rank=r,
                         agent_stride=0 if shared else r)
     check_attn(O, ref, what=f"decode {case} {kernel}")
 
 
-@pytest.mark.parametrize("kernel", ["tensor", "simt"])
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05", "simt"])
 def test_decode_lora_term_alone(kernel):
     """V_base = 0 isolates (P.L_a).B_a, so the LoRA path is checked at full weight."""
     w = small_workload(3, 32, 8, 128, 16)
@@ -113,19 +113,21 @@ def test_decode_f32_tiny_workload():
     check_attn(O, ref, atol=1e-4, rtol_l2=1e-5, what="tiny fp32")
 
 
-def test_decode_llama8b_full():
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+def test_decode_llama8b_full(kernel):
     w = WORKLOADS["llama8b_decode"]
     x = make_decode_inputs(w, seed=0)
-    O = run_decode(x, w.rank, "tensor")
+    O = run_decode(x, w.rank, kernel)
     ref = oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"].numpy(), rank=w.rank)
     check_attn(O, ref, what="llama8b_decode")
 
 
-def test_decode_ragged_sampled_requests():
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+def test_decode_ragged_sampled_requests(kernel):
     """Full 32-request ragged batch on the GPU; 6 requests re-computed by the oracle."""
     w = WORKLOADS["llama8b_ragged"]
     x = make_decode_inputs(w, seed=0)
-    O = run_decode(x, w.rank, "tensor").cpu()
+    O = run_decode(x, w.rank, kernel).cpu()
     offs = x["offsets"].numpy()
     for q in [0, 5, 14, 23, 27, 31]:  # includes the longest (14) and shortest (23) requests
         t0, t1 = int(offs[q]), int(offs[q + 1])
@@ -134,10 +136,11 @@ def test_decode_ragged_sampled_requests():
         check_attn(O[q:q + 1], ref, what=f"ragged request {q}")
 
 
-def test_decode_llama70b_sampled_agents():
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+def test_decode_llama70b_sampled_agents(kernel):
     w = WORKLOADS["llama70b_decode"]
     x = make_decode_inputs(w, seed=0)
-    O = run_decode(x, w.rank, "tensor").cpu()
+    O = run_decode(x, w.rank, kernel).cpu()
     r = w.rank
     for a in [0, 4]:
         ref = oracle.decode(x["Q"][:, a:a + 1], x["K_base"], x["V_base"], x["L"][:, a * r:(a + 1) * r],
@@ -145,14 +148,26 @@ def test_decode_llama70b_sampled_agents():
         check_attn(O[:, a:a + 1], ref, what=f"70b agent {a}")
 
 
-def test_decode_tensor_and_simt_agree_and_are_deterministic():
+@pytest.mark.parametrize("kernel", ["mma", "tcgen05"])
+def test_decode_tensor_and_simt_agree_and_are_deterministic(kernel):
     w = WORKLOADS["llama8b_decode"]
     x = make_decode_inputs(w, seed=3)
-    O1 = run_decode(x, w.rank, "tensor")
-    O2 = run_decode(x, w.rank, "tensor")
-    assert torch.equal(O1, O2), "tensor decode is not deterministic run to run"
+    O1 = run_decode(x, w.rank, kernel)
+    O2 = run_decode(x, w.rank, kernel)
+    assert torch.equal(O1, O2), f"{kernel} decode is not deterministic run to run"
     O3 = run_decode(x, w.rank, "simt")
-    check_attn(O1, O3.double().cpu().numpy(), what="tensor vs simt")
+    check_attn(O1, O3.double().cpu().numpy(), what=f"{kernel} vs simt")
+
+
+def test_decode_tcgen05_rescales_when_scores_jump():
+    """Q scaled so the running max moves by far more than 2^8 between tiles: exercises the rescale
+    of O, OL and l in TMEM; one request shorter than a tile and one empty request ride along."""
+    w = small_workload(5, 40, 8, 128, 16)
+    x = make_decode_inputs(w, seed=21, lengths=[3000, 100, 0, 1300])
+    x["Q"] = (x["Q"].float() * 8.0).to(x["Q"].dtype)
+    O = run_decode(x, 16, "tcgen05")
+    ref = oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"].numpy(), rank=16)
+    check_attn(O, ref, what="tcgen05 rescale")
 
 
 def test_prepared_decode_matches_the_function():
@@ -175,10 +190,11 @@ def test_decode_output_guard_bands():
     n = R * A * hq * d
     buf = torch.full((n + 2048,), 12345.0, device="cuda")
     O = buf[1024:1024 + n].view(R, A, hq, d)
-    _fla().flash_lora_attn_decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"], rank=16,
-                                  O=O, kernel="tensor")
-    torch.cuda.synchronize()
-    assert torch.all(buf[:1024] == 12345.0) and torch.all(buf[1024 + n:] == 12345.0)
+    for kernel in ("mma", "tcgen05"):
+        _fla().flash_lora_attn_decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"], rank=16,
+                                      O=O, kernel=kernel)
+        torch.cuda.synchronize()
+        assert torch.all(buf[:1024] == 12345.0) and torch.all(buf[1024 + n:] == 12345.0)
 
 
 # ----------------------------------------------------------------------------- prefill
