@@ -119,9 +119,10 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const uint32_t red = bar0 + 8u * (4 * kMaxRing + 7);
   const uint32_t drain = bar0 + 8u * (4 * kMaxRing + 8);
 
-  // Launched with programmatic dependent launch: wait for the previous grid in
-  // the stream (it may still read this call's workspace) before writing.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Launched with programmatic dependent launch: the token loop reads only
+  // this call's inputs, so it may overlap the previous kernel of the stream
+  // (this library's merge kernel, which reads the workspace);
+  // griddepcontrol.wait runs before this CTA's first global write.
   if (warp == 0) {
     const int found = dec::map_unit(unit_global, p.unit_tokens, p.single_len, p.offsets, p.n_req, s_info);
     if (lane == 0) s_info[5] = found;
@@ -154,7 +155,6 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (!s_info[5]) return;  // grid slack beyond the last unit (uniform over the CTA)
   const int qreq = s_info[0], unit = s_info[1], n_units = s_info[2];
   const int tok_begin = s_info[3], n_tok = s_info[4];
-  if (unit == 0 && threadIdx.x == 0) p.pair_info[qreq * p.hkv + head] = make_int2(unit_global, n_units);
   const int n = (n_tok + kKeys - 1) / kKeys;  // 128-token tiles of this unit
   // The kv heads of a unit share its L rows.  Head h visits the unit's tiles
   // starting at tile h, so one head pulls each L tile from HBM and the others
@@ -427,6 +427,8 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     // ---- partial record: [rows][d + r] (O | own agent's OL) | m[rows] | l[rows]
     if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_ab(pvdone, (n - 1) & 1, &s_abort));
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (unit == 0 && key == 0) p.pair_info[qreq * p.hkv + head] = make_int2(unit_global, n_units);
     if (ok) {
       const int W = D + p.r;
       float *part = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;

@@ -189,10 +189,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x % p.hkv;
   const int unit_global = blockIdx.x / p.hkv;
-  // Launched with programmatic dependent launch: the CTA may become resident
-  // while the previous kernel in the stream drains; nothing it wrote is read
-  // before this wait returns.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Launched with programmatic dependent launch: the CTA may start while the
+  // previous kernel of the stream (this library's merge or decode kernel)
+  // drains.  The token loop reads only this call's inputs, which that kernel
+  // does not write; griddepcontrol.wait runs before this CTA's first global
+  // write (pair_info, partials, O: the previous call's merge reads the
+  // workspace), so the loop overlaps the previous call's tail.
 
   // ---- map unit_global -> (request, unit) with a warp-parallel scan
   if (warp == 0) {
@@ -218,7 +220,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int tok_begin = s_info[3], n_tok = s_info[4];
   // every (q, head) tells the merge kernel where its units start and how many
   // there are (the workspace is not initialised; single-unit pairs are skipped)
-  if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(unit_global, n_units);
   const int n_tiles = (n_tok + T - 1) / T;
   const uint32_t bar_full0 = ptx::smem_u32(&bars[0]);
   const uint32_t bar_empty0 = ptx::smem_u32(&bars[p.stages]);
@@ -563,6 +564,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       }
     }
     // ---- O = (P.V_base + (P.L_a).B_a) / l, straight from the fragments
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(unit_global, n_units);
     const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
@@ -582,6 +585,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   // ---- several units: publish this unit's partial straight from the
   //      fragments: [rows][D + r] (P.V_base | own agent's P.L_a) | m[rows] | l[rows]
   if (kslice != 0) return;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(unit_global, n_units);
   {
     const int W = D + p.r;
     float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;

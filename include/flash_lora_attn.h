@@ -141,6 +141,12 @@ FLA_API fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, v
  *            results of long contexts between the decode kernel and the merge
  *            kernel the call enqueues behind it; calls that may overlap on the
  *            GPU must use different workspaces.
+ * Ordering: the call's kernels are launched with programmatic dependent
+ * launch, so when the previous work on the stream is this library's decode,
+ * the new call starts reading Q, K_base, V_base, L, B and offsets while that
+ * decode finishes.  Those inputs must not be the O or the workspace of the
+ * decode call enqueued immediately before on the same stream (every other
+ * producer, e.g. a PyTorch kernel, has completed first as usual).
  * Errors: INVALID_ARG (null pointer, hq % hkv, offsets layout on the host
  * side, strides), UNSUPPORTED (shape outside the selected kernel's limits),
  * WORKSPACE (too small), CUDA (launch failure).
