@@ -651,16 +651,9 @@ inline fla_status decode_t5_launch(const fla_attn_dims &d, float scale, const vo
   mp.part_stride = pl.part_stride; mp.unit_tokens = (int)U; mp.single_len = prm.single_len;
   mp.merge_single = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(n_req * d.hkv), (unsigned)pl.rows);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = (size_t)d.rank * dt5::D * 2 + 4 * 32 * (dt5::D / 32 + 4) * 4;
-  if (cfg.dynamicSmemBytes > 48 * 1024) {
-    e = ensure_dynamic_smem(reinterpret_cast<const void *>(dec::decode_merge_kernel<dt5::D>), (int)cfg.dynamicSmemBytes);
-    if (e != cudaSuccess) {
-      decode_tc_err() = cudaGetErrorString(e);
-      return FLA_ERR_CUDA;
-    }
-  }
+  cfg.gridDim = dim3(merge_grid(n_req, d.hkv, pl.rows));
+  cfg.blockDim = dim3(dec::kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = 1;

@@ -618,12 +618,16 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // into units u with partials (m_u, l_u, acc_u = P_u.V_base, pl_u = P_u.L_a):
 //   w_u = 2^(m_u - max_u m_u)          (log2-domain running maxima)
 //   O   = (sum_u w_u acc_u + (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]) / sum_u w_u l_u
-// units combined in order (deterministic).  Grid: (n_req * hkv, ceil(rows/4)),
-// one warp per query row, D/32 columns per lane, sixteen units' loads in
-// flight per step.  Launched with programmatic dependent launch right behind
-// the decode kernel: B is staged before griddepcontrol.wait, which returns
-// once the decode grid has completed and its writes are visible.
+// units combined in order (deterministic).  One warp per query row, D/32
+// columns per lane, four units' loads in flight per step; kMergeWarps rows
+// per CTA, so a handful of CTAs cover a single-request decode and fit on the
+// SMs its decode grid leaves free.  Launched with programmatic dependent
+// launch right behind the decode kernel; griddepcontrol.wait returns once the
+// decode grid has completed and its writes are visible.  The next decode may
+// start its token loop while this decode's tail and this kernel run.
 // ---------------------------------------------------------------------------
+constexpr int kMergeWarps = 32;
+
 struct MergeParams {
   const float *partials;
   const int2 *pair_info;
@@ -634,125 +638,96 @@ struct MergeParams {
 };
 
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(const MergeParams p) {
-  extern __shared__ __align__(16) uint8_t msm[];
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const MergeParams p) {
   constexpr int CPL = D / 32;  // accumulator columns per lane
-  __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(msm);  // [r][D] of this row's agent
-  float *red = reinterpret_cast<float *>(msm + (size_t)p.r * D * 2);  // [4 warps][32 lanes][CPL + 4]
-  const int pair = blockIdx.x;
-  const int q = pair / p.hkv, head = pair % p.hkv;
-  const int row = blockIdx.y;
-  const int a = row / p.G, j = head * p.G + row % p.G;
-  const int r = p.r;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // B_a[:, h*d:(h+1)*d] is an input: stage it before waiting on the decode grid
-  for (int e = threadIdx.x; e < r * (D / 8); e += 128) {
-    const int k = e / (D / 8), c8 = e - k * (D / 8);
-    reinterpret_cast<uint4 *>(Bs)[e] =
-        *reinterpret_cast<const uint4 *>(p.B + ((int64_t)(a * r + k) * p.hkv + head) * D + c8 * 8);
-  }
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the next decode may be scheduled now (it waits for this grid before reading)
+  // The next decode may be scheduled as soon as every CTA of this grid is
+  // resident: its token loop reads only its own inputs and it waits for this
+  // grid before its first global write.  Every grid waited on is then fully
+  // resident (a dependent launches only once all CTAs of its primary have
+  // issued this instruction), so the chain decode -> merge -> decode cannot
+  // deadlock on SM space.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  int ug0, nu;
-  if (p.single_len >= 0) {
-    ug0 = 0;
-    nu = p.single_len > 0 ? (p.single_len + p.unit_tokens - 1) / p.unit_tokens : 1;
-  } else {
-    const int2 info = __ldcg(p.pair_info + pair);
-    ug0 = info.x;
-    nu = info.y;
-  }
-  if (nu <= 1 && !p.merge_single) return;  // written directly by the decode kernel (uniform over the CTA)
-  const int W = D + r;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int total = p.n_req * p.hkv * p.rows;
+  const int W = D + p.r;
   const int64_t ustride = (int64_t)p.hkv * p.part_stride;
-  const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
-  // warp w combines units w, w + 4, ... ; eight of them in flight per step
-  float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  constexpr int CH = 8;
-  for (int u0 = warp; u0 < nu; u0 += 4 * CH) {
-    float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
-#pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      const int u = min(u0 + 4 * k, nu - 1);
-      const float *src = base + u * ustride;
-      mu[k] = __ldcg(src + p.rows * W + row);
-      lu[k] = __ldcg(src + p.rows * W + p.rows + row);
-      if constexpr (CPL == 4) {
-        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * W) + lane);
-        v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
-      } else {
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * W + lane * CPL + c);
-      }
-      a2[k][0] = lane < r ? __ldcg(src + row * W + D + lane) : 0.f;
-      a2[k][1] = lane + 32 < r ? __ldcg(src + row * W + D + 32 + lane) : 0.f;
+  for (int gr = blockIdx.x * kMergeWarps + warp; gr < total; gr += gridDim.x * kMergeWarps) {
+    const int pair = gr / p.rows, row = gr % p.rows;
+    const int q = pair / p.hkv, head = pair % p.hkv;
+    const int a = row / p.G, j = head * p.G + row % p.G;
+    int ug0, nu;
+    if (p.single_len >= 0) {
+      ug0 = 0;
+      nu = p.single_len > 0 ? (p.single_len + p.unit_tokens - 1) / p.unit_tokens : 1;
+    } else {
+      const int2 info = __ldcg(p.pair_info + pair);
+      ug0 = info.x;
+      nu = info.y;
     }
-    float Mc = M;
+    if (nu <= 1 && !p.merge_single) continue;  // written directly by the decode kernel
+    const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
+    float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < CH; ++k)
-      if (u0 + 4 * k < nu) Mc = fmaxf(Mc, mu[k]);
-    const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
-    M = Mc;
-    lsum *= sc;
-    pl[0] *= sc;
-    pl[1] *= sc;
+    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+    constexpr int CH = 4;
+    for (int u0 = 0; u0 < nu; u0 += CH) {
+      float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] *= sc;
+      for (int k = 0; k < CH; ++k) {
+        const int u = min(u0 + k, nu - 1);
+        const float *src = base + u * ustride;
+        mu[k] = __ldcg(src + p.rows * W + row);
+        lu[k] = __ldcg(src + p.rows * W + p.rows + row);
+        if constexpr (CPL == 4) {
+          const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * W) + lane);
+          v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+        } else {
 #pragma unroll
-    for (int k = 0; k < CH; ++k) {
-      if (u0 + 4 * k < nu) {
-        const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
-        lsum += w * lu[k];
+          for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * W + lane * CPL + c);
+        }
+        a2[k][0] = lane < p.r ? __ldcg(src + row * W + D + lane) : 0.f;
+        a2[k][1] = lane + 32 < p.r ? __ldcg(src + row * W + D + 32 + lane) : 0.f;
+      }
+      float Mc = M;
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
-        pl[0] += w * a2[k][0];
-        pl[1] += w * a2[k][1];
+      for (int k = 0; k < CH; ++k)
+        if (u0 + k < nu) Mc = fmaxf(Mc, mu[k]);
+      const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
+      M = Mc;
+      lsum *= sc;
+      pl[0] *= sc;
+      pl[1] *= sc;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[c] *= sc;
+#pragma unroll
+      for (int k = 0; k < CH; ++k) {
+        if (u0 + k < nu) {
+          const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
+          lsum += w * lu[k];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
+          pl[0] += w * a2[k][0];
+          pl[1] += w * a2[k][1];
+        }
       }
     }
+    // (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]: lane k holds pl[k] (and pl[k + 32] when r > 32)
+    float lora[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
+    const __nv_bfloat16 *bcol = p.B + (int64_t)a * p.r * p.hkv * D + head * D + lane * CPL;
+    for (int k = 0; k < p.r; ++k) {
+      const float plk = __shfl_sync(0xffffffffu, k < 32 ? pl[0] : pl[1], k & 31);
+      const __nv_bfloat16 *bk = bcol + (int64_t)k * p.hkv * D;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bk[c]);
+    }
+    float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) out[c] = (acc[c] + lora[c]) * inv;
   }
-  // combine the four warps (fixed order: deterministic)
-  float *my = red + (warp * 32 + lane) * (CPL + 4);
-  my[0] = M;
-  my[1] = lsum;
-  my[2] = pl[0];
-  my[3] = pl[1];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) my[4 + c] = acc[c];
-  __syncthreads();
-  if (warp != 0) return;
-  float Mt = -INFINITY;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) Mt = fmaxf(Mt, red[(w * 32 + lane) * (CPL + 4)]);
-  float ls = 0.f, plt[2] = {0.f, 0.f}, at[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) at[c] = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    const float *o = red + (w * 32 + lane) * (CPL + 4);
-    const float wt = (o[0] == -INFINITY) ? 0.f : ptx::ex2(o[0] - Mt);
-    ls += wt * o[1];
-    plt[0] += wt * o[2];
-    plt[1] += wt * o[3];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) at[c] += wt * o[4 + c];
-  }
-  // (sum_u w_u pl_u) . B_a: lane k holds pl[k] (and pl[k + 32] when r > 32)
-  float lora[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
-  const __nv_bfloat16 *bs = Bs + lane * CPL;
-  for (int k = 0; k < r; ++k) {
-    const float plk = __shfl_sync(0xffffffffu, k < 32 ? plt[0] : plt[1], k & 31);
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bs[k * D + c]);
-  }
-  float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
-  const float inv = ls > 0.f ? 1.f / ls : 0.f;
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) out[c] = (at[c] + lora[c]) * inv;
 }
 
 }  // namespace dec
@@ -915,6 +890,12 @@ inline CUtensorMapSwizzle swizzle_enum(int bytes) {
                       : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
+// CTAs of the merge kernel: one warp per query row.
+inline unsigned merge_grid(int n_req, int hkv, int rows) {
+  const int64_t total = (int64_t)n_req * hkv * rows;
+  return (unsigned)std::max<int64_t>(1, (total + dec::kMergeWarps - 1) / dec::kMergeWarps);
+}
+
 template <int D, int MT, int TG, int NLT, int SG>
 inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, const CUtensorMap &mV,
                                 const CUtensorMap &mL, const CUtensorMap &mB, const dec::Params &prm, unsigned grid,
@@ -952,17 +933,9 @@ inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, con
   mp.r = prm.r;
   mp.part_stride = prm.part_stride; mp.unit_tokens = prm.unit_tokens; mp.single_len = prm.single_len;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(prm.n_req * prm.hkv), (unsigned)prm.rows);
-  cfg.blockDim = dim3(128);
-  // this row's B slice plus the cross-warp reduction buffer
-  cfg.dynamicSmemBytes = (size_t)prm.r * D * 2 + 4 * 32 * (D / 32 + 4) * 4;
-  if (cfg.dynamicSmemBytes > 48 * 1024) {
-    e = ensure_dynamic_smem(reinterpret_cast<const void *>(dec::decode_merge_kernel<D>), (int)cfg.dynamicSmemBytes);
-    if (e != cudaSuccess) {
-      decode_tc_err() = cudaGetErrorString(e);
-      return FLA_ERR_CUDA;
-    }
-  }
+  cfg.gridDim = dim3(merge_grid(prm.n_req, prm.hkv, prm.rows));
+  cfg.blockDim = dim3(dec::kMergeWarps * 32);
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
