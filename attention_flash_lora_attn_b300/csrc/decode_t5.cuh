@@ -650,14 +650,7 @@ inline fla_status decode_t5_launch(const fla_attn_dims &d, float scale, const vo
   mp.r = d.rank;
   mp.part_stride = pl.part_stride; mp.unit_tokens = (int)U; mp.single_len = prm.single_len;
   mp.merge_single = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(merge_grid(n_req, d.hkv, pl.rows));
-  cfg.blockDim = dim3(dec::kMergeWarps * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, dec::decode_merge_kernel<dt5::D>, mp);
+  e = launch_merge<dt5::D>(mp, units, grid64, s);
   if (e != cudaSuccess) {
     decode_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;

@@ -32,7 +32,7 @@
 //   * the SG*TG token slices are merged in shared memory; a CTA that is the only
 //     unit of its (q, h) writes O, otherwise it writes its partial
 //     (m, l, d-wide accumulator) to the workspace;
-//   * decode_merge_kernel, launched right behind with programmatic dependent
+//   * the merge kernel, launched right behind with programmatic dependent
 //     launch (it waits on the grid dependency, no flag polling), combines the
 //     partials of every (q, h) in unit order (deterministic) and writes O: one
 //     warp per query row, every unit's load in flight at once.
@@ -618,15 +618,17 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // into units u with partials (m_u, l_u, acc_u = P_u.V_base, pl_u = P_u.L_a):
 //   w_u = 2^(m_u - max_u m_u)          (log2-domain running maxima)
 //   O   = (sum_u w_u acc_u + (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]) / sum_u w_u l_u
-// units combined in order (deterministic).  One warp per query row, D/32
-// columns per lane, four units' loads in flight per step; kMergeWarps rows
-// per CTA, so a handful of CTAs cover a single-request decode and fit on the
-// SMs its decode grid leaves free.  Launched with programmatic dependent
+// units combined in order (deterministic).  Two geometries: one warp per
+// query row (32 rows per CTA) when the merge fits on the SMs the decode grid
+// leaves idle or the rows have few units; four warps per row otherwise
+// (units split by index and combined in shared memory in fixed order, the
+// agent's B slice staged before the wait; one row per CTA, so the merge
+// spreads over every SM).  Launched with programmatic dependent
 // launch right behind the decode kernel; griddepcontrol.wait returns once the
 // decode grid has completed and its writes are visible.  The next decode may
 // start its token loop while this decode's tail and this kernel run.
 // ---------------------------------------------------------------------------
-constexpr int kMergeWarps = 32;
+constexpr int kMergeWarps = 32;   // warps per CTA
 
 struct MergeParams {
   const float *partials;
@@ -637,8 +639,10 @@ struct MergeParams {
   int32_t merge_single;  // 1: single-unit pairs have a partial too (finish them here)
 };
 
+// One warp per query row, no shared memory or barriers: the geometry for
+// merges that fit on the SMs a decode grid leaves idle, or rows with few units.
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_warp_kernel(const MergeParams p) {
   constexpr int CPL = D / 32;  // accumulator columns per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // The next decode may be scheduled as soon as every CTA of this grid is
@@ -728,6 +732,131 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_kernel(const Me
 #pragma unroll
     for (int c = 0; c < CPL; ++c) out[c] = (acc[c] + lora[c]) * inv;
   }
+}
+
+// Four warps per query row, one row per CTA (the geometry for rows with many
+// units): this row's B_a slice is staged in shared memory before the wait, and
+// the rank is applied by one warp after a fixed-order combine.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_row_kernel(const MergeParams p) {
+  extern __shared__ __align__(16) uint8_t msm[];
+  constexpr int CPL = D / 32;  // accumulator columns per lane
+  __nv_bfloat16 *Bs = reinterpret_cast<__nv_bfloat16 *>(msm);  // [r][D] of this row's agent
+  float *red = reinterpret_cast<float *>(msm + (size_t)p.r * D * 2);  // [4 warps][32 lanes][CPL + 4]
+  const int pair = blockIdx.x;
+  const int q = pair / p.hkv, head = pair % p.hkv;
+  const int row = blockIdx.y;
+  const int a = row / p.G, j = head * p.G + row % p.G;
+  const int r = p.r;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // B_a[:, h*d:(h+1)*d] is an input: stage it before waiting on the decode grid
+  for (int e = threadIdx.x; e < r * (D / 8); e += 128) {
+    const int k = e / (D / 8), c8 = e - k * (D / 8);
+    reinterpret_cast<uint4 *>(Bs)[e] =
+        *reinterpret_cast<const uint4 *>(p.B + ((int64_t)(a * r + k) * p.hkv + head) * D + c8 * 8);
+  }
+  // the next decode may be scheduled now (see decode_merge_warp_kernel)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  int ug0, nu;
+  if (p.single_len >= 0) {
+    ug0 = 0;
+    nu = p.single_len > 0 ? (p.single_len + p.unit_tokens - 1) / p.unit_tokens : 1;
+  } else {
+    const int2 info = __ldcg(p.pair_info + pair);
+    ug0 = info.x;
+    nu = info.y;
+  }
+  if (nu <= 1 && !p.merge_single) return;  // written directly by the decode kernel (uniform over the CTA)
+  const int W = D + r;
+  const int64_t ustride = (int64_t)p.hkv * p.part_stride;
+  const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
+  // warp w combines units w, w + 4, ... ; eight of them in flight per step
+  float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  constexpr int CH = 8;
+  for (int u0 = warp; u0 < nu; u0 += 4 * CH) {
+    float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      const int u = min(u0 + 4 * k, nu - 1);
+      const float *src = base + u * ustride;
+      mu[k] = __ldcg(src + p.rows * W + row);
+      lu[k] = __ldcg(src + p.rows * W + p.rows + row);
+      if constexpr (CPL == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * W) + lane);
+        v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+      } else {
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * W + lane * CPL + c);
+      }
+      a2[k][0] = lane < r ? __ldcg(src + row * W + D + lane) : 0.f;
+      a2[k][1] = lane + 32 < r ? __ldcg(src + row * W + D + 32 + lane) : 0.f;
+    }
+    float Mc = M;
+#pragma unroll
+    for (int k = 0; k < CH; ++k)
+      if (u0 + 4 * k < nu) Mc = fmaxf(Mc, mu[k]);
+    const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
+    M = Mc;
+    lsum *= sc;
+    pl[0] *= sc;
+    pl[1] *= sc;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] *= sc;
+#pragma unroll
+    for (int k = 0; k < CH; ++k) {
+      if (u0 + 4 * k < nu) {
+        const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
+        lsum += w * lu[k];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
+        pl[0] += w * a2[k][0];
+        pl[1] += w * a2[k][1];
+      }
+    }
+  }
+  // combine the four warps (fixed order: deterministic)
+  float *my = red + (warp * 32 + lane) * (CPL + 4);
+  my[0] = M;
+  my[1] = lsum;
+  my[2] = pl[0];
+  my[3] = pl[1];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) my[4 + c] = acc[c];
+  __syncthreads();
+  if (warp != 0) return;
+  float Mt = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) Mt = fmaxf(Mt, red[(w * 32 + lane) * (CPL + 4)]);
+  float ls = 0.f, plt[2] = {0.f, 0.f}, at[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) at[c] = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float *o = red + (w * 32 + lane) * (CPL + 4);
+    const float wt = (o[0] == -INFINITY) ? 0.f : ptx::ex2(o[0] - Mt);
+    ls += wt * o[1];
+    plt[0] += wt * o[2];
+    plt[1] += wt * o[3];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) at[c] += wt * o[4 + c];
+  }
+  // (sum_u w_u pl_u) . B_a: lane k holds pl[k] (and pl[k + 32] when r > 32)
+  float lora[CPL];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
+  const __nv_bfloat16 *bs = Bs + lane * CPL;
+  for (int k = 0; k < r; ++k) {
+    const float plk = __shfl_sync(0xffffffffu, k < 32 ? plt[0] : plt[1], k & 31);
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bs[k * D + c]);
+  }
+  float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
+  const float inv = ls > 0.f ? 1.f / ls : 0.f;
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) out[c] = (at[c] + lora[c]) * inv;
 }
 
 }  // namespace dec
@@ -890,10 +1019,46 @@ inline CUtensorMapSwizzle swizzle_enum(int bytes) {
                       : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
-// CTAs of the merge kernel: one warp per query row.
-inline unsigned merge_grid(int n_req, int hkv, int rows) {
+// Merge-kernel geometry.  One warp per row keeps the CTA count small: when
+// those CTAs fit on the SMs the decode grid leaves idle, they are resident
+// before the decode ends and the next decode's CTAs take every SM the decode
+// frees.  Rows with many units are merged faster by four warps each.
+struct MergeShape {
+  int wpr;
+  unsigned grid;
+};
+inline MergeShape merge_shape(int n_req, int hkv, int rows, int64_t units_total, int64_t decode_grid) {
   const int64_t total = (int64_t)n_req * hkv * rows;
-  return (unsigned)std::max<int64_t>(1, (total + dec::kMergeWarps - 1) / dec::kMergeWarps);
+  const int64_t one = (total + dec::kMergeWarps - 1) / dec::kMergeWarps;
+  const int64_t idle = std::max<int64_t>(0, device_sm_count() - decode_grid);
+  const bool few_units = units_total <= 4 * (int64_t)n_req;
+  if (one <= idle || few_units) return MergeShape{1, (unsigned)std::max<int64_t>(1, one)};
+  return MergeShape{4, (unsigned)total};
+}
+
+// Launches the merge kernel behind a decode kernel (programmatic dependent launch).
+template <int D>
+inline cudaError_t launch_merge(const dec::MergeParams &mp, int64_t units_total, int64_t decode_grid, cudaStream_t s) {
+  const MergeShape ms = merge_shape(mp.n_req, mp.hkv, mp.rows, units_total, decode_grid);
+  cudaLaunchConfig_t cfg = {};
+  // one-warp kernel: a 1-D grid of 32-row CTAs; four-warp kernel: (pair, row)
+  cfg.gridDim = ms.wpr == 1 ? dim3(ms.grid) : dim3((unsigned)(mp.n_req * mp.hkv), (unsigned)mp.rows);
+  cfg.blockDim = dim3(ms.wpr == 1 ? dec::kMergeWarps * 32 : 4 * 32);
+  // the four-warp kernel: this row's B slice plus the cross-warp combine buffer
+  cfg.dynamicSmemBytes = ms.wpr == 1 ? 0 : (size_t)mp.r * D * 2 + 4 * 32 * (D / 32 + 4) * 4;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if (ms.wpr == 1) return cudaLaunchKernelEx(&cfg, dec::decode_merge_warp_kernel<D>, mp);
+  if (cfg.dynamicSmemBytes > 48 * 1024) {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(dec::decode_merge_row_kernel<D>),
+                                              (int)cfg.dynamicSmemBytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaLaunchKernelEx(&cfg, dec::decode_merge_row_kernel<D>, mp);
 }
 
 template <int D, int MT, int TG, int NLT, int SG>
@@ -932,17 +1097,7 @@ inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, con
   mp.n_req = prm.n_req; mp.A = prm.A; mp.hq = prm.hq; mp.hkv = prm.hkv; mp.G = prm.G; mp.rows = prm.rows;
   mp.r = prm.r;
   mp.part_stride = prm.part_stride; mp.unit_tokens = prm.unit_tokens; mp.single_len = prm.single_len;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(merge_grid(prm.n_req, prm.hkv, prm.rows));
-  cfg.blockDim = dim3(dec::kMergeWarps * 32);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = s;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, dec::decode_merge_kernel<D>, mp);
+  e = launch_merge<D>(mp, grid / prm.hkv, grid, s);
   if (e != cudaSuccess) {
     decode_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;
