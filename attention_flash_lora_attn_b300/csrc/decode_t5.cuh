@@ -154,7 +154,7 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!s_info[5]) return;  // grid slack beyond the last unit (uniform over the CTA)
   const int qreq = s_info[0], unit = s_info[1], n_units = s_info[2];
-  const int tok_begin = s_info[3], n_tok = s_info[4];
+  const int tok_begin = s_info[3], n_tok = s_info[4], slot = s_info[6];
   const int n = (n_tok + kKeys - 1) / kKeys;  // 128-token tiles of this unit
   // The kv heads of a unit share its L rows.  Head h visits the unit's tiles
   // starting at tile h, so one head pulls each L tile from HBM and the others
@@ -428,10 +428,10 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     // ---- partial record: [rows][d + r] (O | own agent's OL) | m[rows] | l[rows]
     if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_ab(pvdone, (n - 1) & 1, &s_abort));
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (unit == 0 && key == 0) p.pair_info[qreq * p.hkv + head] = make_int2(unit_global, n_units);
+    if (unit == 0 && key == 0) p.pair_info[qreq * p.hkv + head] = make_int2(slot - unit, n_units);
     if (ok) {
       const int W = D + p.r;
-      float *part = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;
+      float *part = p.partials + ((int64_t)slot * p.hkv + head) * p.part_stride;
       if (n > 0) {
         ptx::tc_fence_after();
         uint32_t ov[kN];

@@ -9,8 +9,9 @@
 //
 // Work decomposition.  A work item is (request q, kv head h, unit u): a
 // contiguous range of at most `unit_tokens` tokens of request q.  One CTA per
-// work item; the CTA index is unit_global * hkv + h so the kv heads of the same
-// token range run side by side and share the L tile through L2.
+// work item; the CTA index is unit * hkv + h so the kv heads of the same token
+// range run side by side and share the L tile through L2 (map_unit gives the
+// unit order).
 //
 // Inside a CTA (SG x MT x TG warps, no dedicated producer warp):
 //   * the A*G query rows of kv head h (agent-major: row = a*G + g) are cut into
@@ -113,56 +114,121 @@ __device__ __forceinline__ uint32_t pack_hi_lo(float x0, float x1, uint32_t &lo)
   return (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
 }
 
-// Maps a global unit index to (request q, unit u of q, units of q, first
-// token, token count) in s_info[0..4]; returns whether the unit exists.  Run by
-// one whole warp: a prefix scan of the requests' unit counts, 32 at a time.
-// A request of length len has max(1, ceil(len / U)) units (an empty request
-// still gets one, which writes its zero output).
+// Maps a CTA's unit index (its position in the launch order) to s_info:
+// [0] request q, [1] unit u of q, [2] units of q, [3] first token, [4] token
+// count, [6] partial-record slot.  Returns whether the unit exists.  Run by one
+// whole warp.  A request of length len has nu = max(1, ceil(len / U)) units;
+// the slots of its units are contiguous (request-major), which is how the
+// merge kernel finds them.
+// Launch order (several requests): first every unit but the last of each
+// request (all exactly U tokens, request order), then the last units, the
+// larger first (a warp sort within each group of 32 requests), so the
+// remainders fill the final wave and the grid ends on its shortest units.
 __device__ __forceinline__ int map_unit(int unit_global, int U, int single_len, const int32_t *offsets, int n_req,
                                         int *s_info) {
   const int lane = threadIdx.x & 31;
-  int base = 0, found = 0;
   if (single_len >= 0) {  // one request: its length is known, no scan
     const int len = single_len;
     const int nu = len > 0 ? (len + U - 1) / U : 1;
-    found = unit_global < nu;
+    const int found = unit_global < nu;
     if (found && lane == 0) {
       s_info[0] = 0;
       s_info[1] = unit_global;
       s_info[2] = nu;
       s_info[3] = unit_global * U;
       s_info[4] = len > 0 ? min(U, len - unit_global * U) : 0;
+      s_info[6] = unit_global;
     }
+    return found;
   }
-  for (int q0 = 0; q0 < n_req && !found; q0 += 32) {
+  auto units_of = [&](int q, int &len) {
+    len = offsets[q + 1] - offsets[q];
+    return len > 0 ? (len + U - 1) / U : 1;
+  };
+  // ---- pass 1: full units (all but each request's last), request order
+  int base_f = 0, base_n = 0;
+  for (int q0 = 0; q0 < n_req; q0 += 32) {
     const int q = q0 + lane;
     int len = 0, nu = 0;
-    if (q < n_req) {
-      len = offsets[q + 1] - offsets[q];
-      nu = len > 0 ? (len + U - 1) / U : 1;
-    }
-    int incl = nu;
+    if (q < n_req) nu = units_of(q, len);
+    const int f = q < n_req ? nu - 1 : 0;
+    int incl_f = f, incl_n = nu;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
+      const int vf = __shfl_up_sync(0xffffffffu, incl_f, o), vn = __shfl_up_sync(0xffffffffu, incl_n, o);
+      if (lane >= o) {
+        incl_f += vf;
+        incl_n += vn;
+      }
     }
-    const int excl = base + incl - nu;
-    const bool mine = (q < n_req) && unit_global >= excl && unit_global < excl + nu;
+    const int excl_f = base_f + incl_f - f, excl_n = base_n + incl_n - nu;
+    const bool mine = (q < n_req) && unit_global >= excl_f && unit_global < excl_f + f;
     if (__ballot_sync(0xffffffffu, mine)) {
-      found = 1;
       if (mine) {
-        const int u = unit_global - excl;
+        const int u = unit_global - excl_f;
         s_info[0] = q;
         s_info[1] = u;
         s_info[2] = nu;
         s_info[3] = offsets[q] + u * U;
-        s_info[4] = len > 0 ? min(U, len - u * U) : 0;
+        s_info[4] = U;
+        s_info[6] = excl_n + u;
       }
+      return 1;
     }
-    base += __shfl_sync(0xffffffffu, incl, 31);
+    base_f += __shfl_sync(0xffffffffu, incl_f, 31);
+    base_n += __shfl_sync(0xffffffffu, incl_n, 31);
   }
-  return found;
+  // ---- pass 2: the last unit of every request, larger first within each group of 32
+  const int k = unit_global - base_f;
+  if (k >= n_req) return 0;  // grid slack
+  const int grp = k / 32, rank = k % 32;
+  int slot_base = 0;  // units of the requests before this group
+  for (int q0 = 0; q0 < grp * 32; q0 += 32) {
+    int len, nu = 0;
+    if (q0 + lane < n_req) nu = units_of(q0 + lane, len);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) nu += __shfl_xor_sync(0xffffffffu, nu, o);
+    slot_base += nu;
+  }
+  const int q = grp * 32 + lane;
+  int len = 0, nu = 0, size = -1;
+  if (q < n_req) {
+    nu = units_of(q, len);
+    size = len - (nu - 1) * U;  // 0 for an empty request
+  }
+  int incl_n = nu;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl_n, o);
+    if (lane >= o) incl_n += v;
+  }
+  const int slot_last = slot_base + incl_n - 1;  // slot of this request's last unit
+  // bitonic sort of (size, request) keys, descending size, ascending request on ties
+  unsigned long long key = ((unsigned long long)(uint32_t)(size + 1) << 32) | (uint32_t)(0xffffffffu - (uint32_t)q);
+#pragma unroll
+  for (int k2 = 2; k2 <= 32; k2 <<= 1)
+#pragma unroll
+    for (int j = k2 >> 1; j > 0; j >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, j);
+      const bool desc = (lane & k2) == 0 || k2 == 32;
+      const bool lower = (lane & j) == 0;
+      key = (desc == lower) ? (key > other ? key : other) : (key < other ? key : other);
+    }
+  const unsigned long long pick = __shfl_sync(0xffffffffu, key, rank);
+  const int qs = (int)(0xffffffffu - (uint32_t)(pick & 0xffffffffull));
+  const int src = qs - grp * 32;
+  const int nus = __shfl_sync(0xffffffffu, nu, src);
+  const int sizes = __shfl_sync(0xffffffffu, size, src);
+  const int slots = __shfl_sync(0xffffffffu, slot_last, src);
+  if (lane == 0) {
+    s_info[0] = qs;
+    s_info[1] = nus - 1;
+    s_info[2] = nus;
+    s_info[3] = offsets[qs] + (nus - 1) * U;
+    s_info[4] = sizes;
+    s_info[6] = slots;
+  }
+  return 1;
 }
 
 template <int D, int MT, int TG, int NLT, int SG>
@@ -217,7 +283,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (!s_info[5]) return;  // grid slack beyond the last unit
   const int q = s_info[0], unit = s_info[1], n_units = s_info[2];
-  const int tok_begin = s_info[3], n_tok = s_info[4];
+  const int tok_begin = s_info[3], n_tok = s_info[4], slot = s_info[6];
   // every (q, head) tells the merge kernel where its units start and how many
   // there are (the workspace is not initialised; single-unit pairs are skipped)
   const int n_tiles = (n_tok + T - 1) / T;
@@ -565,7 +631,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     }
     // ---- O = (P.V_base + (P.L_a).B_a) / l, straight from the fragments
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(unit_global, n_units);
+    if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(slot - unit, n_units);
     const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
@@ -586,10 +652,10 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   //      fragments: [rows][D + r] (P.V_base | own agent's P.L_a) | m[rows] | l[rows]
   if (kslice != 0) return;
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(unit_global, n_units);
+  if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(slot - unit, n_units);
   {
     const int W = D + p.r;
-    float *dst = p.partials + ((int64_t)unit_global * p.hkv + head) * p.part_stride;
+    float *dst = p.partials + ((int64_t)slot * p.hkv + head) * p.part_stride;
 #pragma unroll
     for (int h2 = 0; h2 < 2; ++h2) {
       const int row = h2 ? row1 : row0;
