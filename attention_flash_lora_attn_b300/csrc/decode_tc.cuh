@@ -787,11 +787,34 @@ __global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_warp_kernel(con
 #pragma unroll
     for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
     const __nv_bfloat16 *bcol = p.B + (int64_t)a * p.r * p.hkv * D + head * D + lane * CPL;
-    for (int k = 0; k < p.r; ++k) {
-      const float plk = __shfl_sync(0xffffffffu, k < 32 ? pl[0] : pl[1], k & 31);
-      const __nv_bfloat16 *bk = bcol + (int64_t)k * p.hkv * D;
+    // eight rows of B in flight at a time (each lane reads its CPL columns)
+    constexpr int KB = 8;
+    for (int k0 = 0; k0 < p.r; k0 += KB) {
+      __nv_bfloat16 bv[KB][CPL];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bk[c]);
+      for (int i = 0; i < KB; ++i) {
+        const int k = min(k0 + i, p.r - 1);
+        const __nv_bfloat16 *bk = bcol + (int64_t)k * p.hkv * D;
+        if constexpr (CPL == 4) {
+          const uint2 t = __ldg(reinterpret_cast<const uint2 *>(bk));
+          bv[i][0] = __ushort_as_bfloat16((unsigned short)(t.x & 0xffffu));
+          bv[i][1] = __ushort_as_bfloat16((unsigned short)(t.x >> 16));
+          bv[i][2] = __ushort_as_bfloat16((unsigned short)(t.y & 0xffffu));
+          bv[i][3] = __ushort_as_bfloat16((unsigned short)(t.y >> 16));
+        } else {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) bv[i][c] = bk[c];
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < KB; ++i) {
+        const int k = k0 + i;
+        const float plk = __shfl_sync(0xffffffffu, k < 32 ? pl[0] : pl[1], k & 31);
+        if (k < p.r) {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bv[i][c]);
+        }
+      }
     }
     float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
