@@ -971,7 +971,13 @@ struct DecodePlan {
   bool ok;
 };
 
-inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
+// two_per_sm: a single-row-tile shape may use one warp group and at most
+// kTwoPerSmBudget bytes of shared memory, so two CTAs share an SM (a CTA's
+// setup, first loads and epilogue then overlap its neighbour's token loop);
+// this pays off when the grid spans several waves.
+constexpr int kTwoPerSmBudget = 110 * 1024;
+
+inline DecodePlan decode_tc_plan(const fla_attn_dims &d, bool two_per_sm = false) {
   DecodePlan pl{};
   pl.ok = false;
   if (d.dtype != FLA_BF16) return pl;
@@ -1000,9 +1006,12 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
   else return pl;
   // eight warps (two per scheduler) where the row tiles allow it; a single row
   // tile uses two warp groups on alternate 64-token stages (more, smaller
-  // stages in flight than one group of eight on 128-token stages)
+  // stages in flight than one group of eight on 128-token stages), or one
+  // group of four in the two-CTAs-per-SM layout
+  const bool two = two_per_sm && MT == 1;
   const int TG = MT <= 2 ? 4 : 2;
-  const int SG = MT == 1 ? 2 : 1;
+  const int SG = (MT == 1 && !two) ? 2 : 1;
+  const int budget = two ? kTwoPerSmBudget : dec::kSmemBudget;
   const int T = TG * dec::kTW;
   const int stage = 2 * T * D * 2 + T * l_width * 2;
   const int q_bytes = MT * 16 * (D * 2 + 16);
@@ -1017,13 +1026,13 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d) {
   // region, prefetched at kernel start, when that costs no stage; otherwise
   // they are loaded into the ring after the token loop
   auto fit = [&](bool ded, int &st, int &smem) {
-    st = (dec::kSmemBudget - fixed - (ded ? bs_bytes : 0)) / stage;
+    st = (budget - fixed - (ded ? bs_bytes : 0)) / stage;
     if (st > 8) st = 8;
     st -= st % SG;  // each group owns every SG-th stage
     if (st < 2) st = 2;
     while (st * stage < std::max(ring_min, ded ? 0 : bs_bytes)) st += SG;
     smem = st * stage + (ded ? bs_bytes : 0) + fixed;
-    return smem <= 227 * 1024;
+    return smem <= (two ? kTwoPerSmBudget : 227 * 1024);
   };
   int st_plain, sm_plain, st_ded, sm_ded;
   const bool ok_plain = fit(false, st_plain, sm_plain);
@@ -1198,7 +1207,7 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
                                    const void *V, const void *L, const void *B, const int32_t *offsets,
                                    int n_req, int64_t total_tokens, float *O, void *workspace,
                                    cudaStream_t s) {
-  const DecodePlan pl = decode_tc_plan(d);
+  DecodePlan pl = decode_tc_plan(d);
   if (!pl.ok) {
     decode_tc_err() = "shape outside the tensor-core decode kernel";
     return FLA_ERR_UNSUPPORTED;
@@ -1210,6 +1219,11 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
   }
   const int64_t U = decode_unit_tokens(n_req, total_tokens, d.hkv);
   const int64_t units = decode_max_units(n_req, total_tokens, U);
+  if (units * d.hkv > 2 * (int64_t)device_sm_count()) {
+    // several waves of CTAs: two per SM where the shape allows
+    const DecodePlan two = decode_tc_plan(d, true);
+    if (two.ok && two.SG == 1 && two.MT == 1) pl = two;
+  }
   CUtensorMap mK, mV, mL, mB;
   {
     const cuuint64_t dims[3] = {(cuuint64_t)d.head_dim, (cuuint64_t)d.hkv, (cuuint64_t)total_tokens};
@@ -1281,10 +1295,12 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
   if (pl.D == DD && pl.MT == MM && pl.TG == TT && pl.NLT == NN && pl.SG == GG)              \
     return decode_tc_run<DD, MM, TT, NN, GG>(pl, mK, mV, mL, mB, prm, grid, need_merge, s);
   FLA_DEC_CASE(128, 1, 4, 8, 2) FLA_DEC_CASE(128, 1, 4, 16, 2)
+  FLA_DEC_CASE(128, 1, 4, 8, 1) FLA_DEC_CASE(128, 1, 4, 16, 1)
   FLA_DEC_CASE(128, 2, 4, 8, 1) FLA_DEC_CASE(128, 2, 4, 16, 1)
   FLA_DEC_CASE(128, 3, 2, 8, 1) FLA_DEC_CASE(128, 3, 2, 16, 1)
   FLA_DEC_CASE(128, 4, 2, 8, 1) FLA_DEC_CASE(128, 4, 2, 16, 1)
   FLA_DEC_CASE(64, 1, 4, 8, 2) FLA_DEC_CASE(64, 1, 4, 16, 2)
+  FLA_DEC_CASE(64, 1, 4, 8, 1) FLA_DEC_CASE(64, 1, 4, 16, 1)
   FLA_DEC_CASE(64, 2, 4, 8, 1) FLA_DEC_CASE(64, 2, 4, 16, 1)
   FLA_DEC_CASE(64, 3, 2, 8, 1) FLA_DEC_CASE(64, 3, 2, 16, 1)
   FLA_DEC_CASE(64, 4, 2, 8, 1) FLA_DEC_CASE(64, 4, 2, 16, 1)

@@ -159,6 +159,17 @@ def test_decode_tensor_and_simt_agree_and_are_deterministic(kernel):
     check_attn(O1, O3.double().cpu().numpy(), what=f"{kernel} vs simt")
 
 
+def test_decode_many_waves_two_ctas_per_sm():
+    """40 requests: the grid spans several waves, so the mma.sync decode runs two CTAs per SM (one
+    warp group each); the 8B shapes with a 48-column L window."""
+    w = small_workload(3, 32, 8, 128, 16)
+    lengths = [int(v) for v in np.random.default_rng(7).integers(1, 4000, size=40)]
+    x = make_decode_inputs(w, seed=17, lengths=lengths)
+    O = run_decode(x, 16, "mma")
+    ref = oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"].numpy(), rank=16)
+    check_attn(O, ref, what="many waves")
+
+
 def test_decode_tcgen05_rescales_when_scores_jump():
     """Q scaled so the running max moves by far more than 2^8 between tiles: exercises the rescale
     of O, OL and l in TMEM; one request shorter than a tile and one empty request ride along."""
