@@ -101,12 +101,14 @@ struct Cfg {
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kRowsPad = MT * 16;
   static constexpr int kQPitch = D * 2 + 16;  // bytes per Q row in shared memory
-  // per-warp merge scratch: 16 rows x (D accumulators + own agent's P.L_a,
-  // at most the window width), row pitch padded by 8 against bank
-  // conflicts, then m[16], l[16]
-  static constexpr int kSPitch = D + (NLT * 8 < 64 ? NLT * 8 : 64) + 8;
-  static constexpr int kScratchFloats = 16 * kSPitch + 32;
 };
+
+// Floats of the slice-merge exchange (aliased onto the stage ring after the
+// token loop): every warp's fragments and running max / sum, then the merged
+// max and sum of each row tile.
+__host__ __device__ constexpr int merge_exchange_floats(int D, int MT, int TG, int NLT, int SG) {
+  return MT * TG * SG * ((D / 8) * 4 + NLT * 4 + 4) * 32 + MT * 4 * 32;
+}
 
 __device__ __forceinline__ uint32_t pack_hi_lo(float x0, float x1, uint32_t &lo) {
   const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
@@ -522,71 +524,96 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
   const bool single = (n_units == 1);
 
-  // ---- merge the SG*TG token slices of each row tile in registers: a tree
-  //      over the slices; in each round the upper half of the slices writes
-  //      its fragments (thread-linear, conflict-free) into the free ring and
-  //      the lower half combines them with its own.  Slice 0 of each row tile
-  //      ends up holding the tile's state.
+  // ---- merge the SG*TG token slices of each row tile in one pass: every warp
+  //      publishes its fragments into the free ring (one float4 per n-tile and
+  //      lane, thread-linear, conflict-free); after one barrier each warp
+  //      combines a strided share of the n-tiles over all slices of its row
+  //      tile and writes the result into the slot of the tile's slice 0.  The
+  //      tile's running max and row sum go to a small table after the slots.
   constexpr int NS = C::kSlices;
-  constexpr int NV = (D / 8) * 4 + NLT * 4 + 4;  // acc_v | acc_l | m0 m1 l0 l1, per thread
-  const int kslice = grp * TG + tg;               // this warp's slice within its row tile
+  constexpr int NQ = D / 8 + NLT;  // float4 groups per lane: acc_v n-tiles | acc_l n-tiles
+  constexpr int NV4 = NQ + 1;      // + (m0, m1, l0, l1)
+  static_assert(NQ % NS == 0, "slices must divide the n-tile count");
+  const int kslice = grp * TG + tg;  // this warp's slice within its row tile
+  float4 *xch = reinterpret_cast<float4 *>(smem);  // [warp][NV4][32 lanes]
+  float4 *mlx = xch + C::kWarps * NV4 * 32;        // [row tile][32 lanes]: merged (M0, M1, L0, L1)
+  auto slice_warp = [&](int k) { return (k / TG) * C::kGroupWarps + mt * TG + (k % TG); };
   {
-    float *xch = reinterpret_cast<float *>(smem);  // [warp][NV][32 lanes]
-#pragma unroll 1
-    for (int half = NS / 2; half >= 1; half /= 2) {
-      if (kslice >= half && kslice < 2 * half) {
-        float *dst = xch + warp * NV * 32 + lane;
+    float4 *dst = xch + warp * NV4 * 32 + lane;
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i)
+    for (int i = 0; i < D / 8; ++i) dst[i * 32] = make_float4(acc_v[i][0], acc_v[i][1], acc_v[i][2], acc_v[i][3]);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) dst[(i * 4 + c) * 32] = acc_v[i][c];
+    for (int i = 0; i < NLT; ++i)
+      dst[(D / 8 + i) * 32] = make_float4(acc_l[i][0], acc_l[i][1], acc_l[i][2], acc_l[i][3]);
+    dst[NQ * 32] = make_float4(m0, m1, l0, l1);
+  }
+  __syncthreads();
+  {
+    float f0[NS], f1[NS];
+    float M0 = -INFINITY, M1 = -INFINITY;
 #pragma unroll
-        for (int i = 0; i < NLT; ++i)
+    for (int k = 0; k < NS; ++k) {
+      const float4 ml = xch[(slice_warp(k) * NV4 + NQ) * 32 + lane];
+      f0[k] = ml.x;
+      f1[k] = ml.y;
+      M0 = fmaxf(M0, ml.x);
+      M1 = fmaxf(M1, ml.y);
+    }
 #pragma unroll
-          for (int c = 0; c < 4; ++c) dst[((D / 8) * 4 + i * 4 + c) * 32] = acc_l[i][c];
-        dst[(NV - 4) * 32] = m0;
-        dst[(NV - 3) * 32] = m1;
-        dst[(NV - 2) * 32] = l0;
-        dst[(NV - 1) * 32] = l1;
+    for (int k = 0; k < NS; ++k) {
+      f0[k] = (f0[k] == -INFINITY) ? 0.f : ptx::ex2(f0[k] - M0);
+      f1[k] = (f1[k] == -INFINITY) ? 0.f : ptx::ex2(f1[k] - M1);
+    }
+#pragma unroll
+    for (int jj = 0; jj < NQ / NS; ++jj) {
+      const int i = jj * NS + kslice;  // fragment elements x, y: row g; z, w: row g + 8
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < NS; ++k) {
+        const float4 v = xch[(slice_warp(k) * NV4 + i) * 32 + lane];
+        acc.x = fmaf(f0[k], v.x, acc.x);
+        acc.y = fmaf(f0[k], v.y, acc.y);
+        acc.z = fmaf(f1[k], v.z, acc.z);
+        acc.w = fmaf(f1[k], v.w, acc.w);
       }
-      __syncthreads();
-      if (kslice < half) {
-        const int k2 = kslice + half;
-        const int pw = (k2 / TG) * C::kGroupWarps + mt * TG + (k2 % TG);  // partner warp
-        const float *src = xch + pw * NV * 32 + lane;
-        const float pm0 = src[(NV - 4) * 32], pm1 = src[(NV - 3) * 32];
-        const float M0 = fmaxf(m0, pm0), M1 = fmaxf(m1, pm1);
-        const float a0 = (m0 == -INFINITY) ? 0.f : ptx::ex2(m0 - M0);
-        const float b0 = (pm0 == -INFINITY) ? 0.f : ptx::ex2(pm0 - M0);
-        const float a1 = (m1 == -INFINITY) ? 0.f : ptx::ex2(m1 - M1);
-        const float b1 = (pm1 == -INFINITY) ? 0.f : ptx::ex2(pm1 - M1);
+      xch[(slice_warp(0) * NV4 + i) * 32 + lane] = acc;  // n-tile i is read and written by this warp alone
+    }
+    if (kslice == 0) {
+      float L0 = 0.f, L1 = 0.f;
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-          acc_v[i][0] = a0 * acc_v[i][0] + b0 * src[(i * 4 + 0) * 32];
-          acc_v[i][1] = a0 * acc_v[i][1] + b0 * src[(i * 4 + 1) * 32];
-          acc_v[i][2] = a1 * acc_v[i][2] + b1 * src[(i * 4 + 2) * 32];
-          acc_v[i][3] = a1 * acc_v[i][3] + b1 * src[(i * 4 + 3) * 32];
-        }
-#pragma unroll
-        for (int i = 0; i < NLT; ++i) {
-          const int o = (D / 8) * 4 + i * 4;
-          acc_l[i][0] = a0 * acc_l[i][0] + b0 * src[(o + 0) * 32];
-          acc_l[i][1] = a0 * acc_l[i][1] + b0 * src[(o + 1) * 32];
-          acc_l[i][2] = a1 * acc_l[i][2] + b1 * src[(o + 2) * 32];
-          acc_l[i][3] = a1 * acc_l[i][3] + b1 * src[(o + 3) * 32];
-        }
-        l0 = a0 * l0 + b0 * src[(NV - 2) * 32];
-        l1 = a1 * l1 + b1 * src[(NV - 1) * 32];
-        m0 = M0;
-        m1 = M1;
+      for (int k = 0; k < NS; ++k) {
+        const float4 ml = xch[(slice_warp(k) * NV4 + NQ) * 32 + lane];
+        L0 = fmaf(f0[k], ml.z, L0);
+        L1 = fmaf(f1[k], ml.w, L1);
       }
-      ptx::fence_proxy_async_smem();  // the ring may next be written by TMA (the B slices)
-      __syncthreads();
+      mlx[mt * 32 + lane] = make_float4(M0, M1, L0, L1);
     }
   }
+  __syncthreads();
 
   const int row0 = row_lo + g, row1 = row_lo + g + 8;
   if (single) {
+    if (kslice == 0) {
+      const float4 *src = xch + warp * NV4 * 32 + lane;
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        const float4 v = src[i * 32];
+        acc_v[i][0] = v.x; acc_v[i][1] = v.y; acc_v[i][2] = v.z; acc_v[i][3] = v.w;
+      }
+#pragma unroll
+      for (int i = 0; i < NLT; ++i) {
+        const float4 v = src[(D / 8 + i) * 32];
+        acc_l[i][0] = v.x; acc_l[i][1] = v.y; acc_l[i][2] = v.z; acc_l[i][3] = v.w;
+      }
+      const float4 ml = mlx[mt * 32 + lane];
+      l0 = ml.z;
+      l1 = ml.w;
+    }
+    if (!p.bs_dedicated) {
+      // the B slices are staged in the ring the fragments were just read from
+      ptx::fence_proxy_async_smem();
+      __syncthreads();
+    }
     // ---- B slices: prefetched at the start, or loaded now into the free ring
     uint8_t *bs = p.bs_dedicated ? bsm : smem;
     if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
@@ -648,32 +675,31 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     return;
   }
 
-  // ---- several units: publish this unit's partial straight from the
-  //      fragments: [rows][D + r] (P.V_base | own agent's P.L_a) | m[rows] | l[rows]
-  if (kslice != 0) return;
+  // ---- several units: publish this unit's partial from the merged slots in
+  //      record order, a row per warp and consecutive columns per lane:
+  //      [rows][D + r] (P.V_base | own agent's P.L_a) | m[rows] | l[rows]
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(slot - unit, n_units);
   {
     const int W = D + p.r;
     float *dst = p.partials + ((int64_t)slot * p.hkv + head) * p.part_stride;
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int row = h2 ? row1 : row0;
-      if (row >= p.rows) continue;
+    const float *xf = reinterpret_cast<const float *>(xch);
+    for (int row = warp; row < p.rows; row += C::kWarps) {
+      const int tile = row >> 4, hi = (row >> 3) & 1, gg = row & 7;
+      // slot of the tile's slice 0 (warp tile * TG of group 0), as floats
+      const float *src = xf + tile * TG * NV4 * 32 * 4;
+      // own agent's first column within the tile's L window
+      const int blk = (row / p.G - (tile * 16) / p.G) * p.l_agent_stride;
       float *drow = dst + row * W;
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i)
-        *reinterpret_cast<float2 *>(drow + i * 8 + 2 * t4) = make_float2(acc_v[i][2 * h2], acc_v[i][2 * h2 + 1]);
-      const int blk = (row / p.G - a_lo) * p.l_agent_stride;  // own block's first window column
-#pragma unroll
-      for (int i = 0; i < NLT; ++i) {
-        const int c = i * 8 + 2 * t4;
-        if (c >= blk && c + 1 < blk + p.r)
-          *reinterpret_cast<float2 *>(drow + D + c - blk) = make_float2(acc_l[i][2 * h2], acc_l[i][2 * h2 + 1]);
+      for (int col = lane; col < W; col += 32) {
+        const int cc = col < D ? col : blk + col - D;
+        const int i = col < D ? (cc >> 3) : D / 8 + (cc >> 3);
+        drow[col] = src[(i * 32 + gg * 4 + ((cc & 7) >> 1)) * 4 + hi * 2 + (cc & 1)];
       }
-      if (t4 == 0) {
-        dst[p.rows * W + row] = h2 ? m1 : m0;
-        dst[p.rows * W + p.rows + row] = h2 ? l1 : l0;
+      if (lane == 0) {
+        const float4 ml = mlx[tile * 32 + gg * 4];
+        dst[p.rows * W + row] = hi ? ml.y : ml.x;
+        dst[p.rows * W + p.rows + row] = hi ? ml.w : ml.z;
       }
     }
   }
@@ -1015,12 +1041,9 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d, bool two_per_sm = false
   const int T = TG * dec::kTW;
   const int stage = 2 * T * D * 2 + T * l_width * 2;
   const int q_bytes = MT * 16 * (D * 2 + 16);
-  // epilogue regions (floats), aliased onto the stage ring after the main loop
-  const int scratch = MT * TG * SG * (16 * (D + std::min(NLT * 8, 64) + 8) + 32);
-  const int tg_merge = rows * (D + r + 2) + ((rows * TG * SG + 3) & ~3);
-  const int part_bytes = ((rows * (D + r + 2) + 3) & ~3) * 4;
+  // the slice-merge exchange is aliased onto the stage ring after the main loop
   const int bs_bytes = d.n_agents * r * D * 2;
-  const int ring_min = std::max({(scratch + tg_merge) * 4, part_bytes, 2 * stage});
+  const int ring_min = std::max(dec::merge_exchange_floats(D, MT, TG, NLT, SG) * 4, 2 * stage);
   const int fixed = q_bytes + (2 * 8 + 2) * 8 + 1024;
   // B slices (needed in this kernel only by single-unit contexts) get their own
   // region, prefetched at kernel start, when that costs no stage; otherwise
