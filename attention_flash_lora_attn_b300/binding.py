@@ -27,7 +27,8 @@ STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "F
 # Every symbol the header declares (tests check that the library exports them).
 EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
             "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
-            "fla_last_error_message", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc")
+            "fla_last_error_message", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc",
+            "lora_value_expand")
 
 
 class FlaError(RuntimeError):
@@ -79,6 +80,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fla_version.restype = ctypes.c_char_p
         lib.flash_lora_attn_decode_noalloc.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, i64, vp, vp]
         lib.flash_lora_attn_decode_noalloc.restype = ctypes.c_int
+        lib.lora_value_expand.argtypes = [dims_p, vp, vp, vp, i64, vp, vp]
+        lib.lora_value_expand.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -273,6 +276,38 @@ def flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0: int, *, rank: int,
     _check(lib.flash_lora_attn_prefill(ctypes.byref(dims), Q.data_ptr(), K_base.data_ptr(), V_base.data_ptr(),
                                        L.data_ptr(), B.data_ptr(), n0, c, O.data_ptr(), ws_ptr, ws_bytes, sp))
     return O
+
+
+def lora_value_expand(V_base, L, B, *, rank: int, l_agent_stride: Optional[int] = None,
+                      V_out: Optional[torch.Tensor] = None, kernel: str = "auto", stream=None) -> torch.Tensor:
+    """Every agent's materialised value cache V_i = V_base + L_i . B_i (the form
+    the reordered attention avoids; used by the naive-materialisation baseline).
+
+    V_base [N, Hkv, d]; L [N, ldL] (unit column stride); B [A, r, Hkv*d].
+    Returns V_out [A, N, Hkv, d] in V_base's dtype.
+    """
+    lib = load_library()
+    _need_cuda(V_base, L, B, V_out)
+    _dense(V_base, "V_base")
+    _dense(B, "B")
+    if L.stride(1) != 1:
+        raise ValueError("L must have unit column stride")
+    N, hkv, d = V_base.shape
+    A = B.shape[0]
+    if tuple(B.shape) != (A, rank, hkv * d):
+        raise ValueError("B must be [A, r, Hkv*d]")
+    if not (V_base.dtype == L.dtype == B.dtype):
+        raise TypeError("V_base, L and B must share one dtype")
+    if l_agent_stride is None:
+        l_agent_stride = rank
+    if V_out is None:
+        V_out = torch.empty((A, N, hkv, d), dtype=V_base.dtype, device=V_base.device)
+    elif tuple(V_out.shape) != (A, N, hkv, d) or V_out.dtype != V_base.dtype or not V_out.is_contiguous():
+        raise ValueError("V_out must be a contiguous [A, N, Hkv, d] tensor of V_base's dtype")
+    dims = make_dims(A, hkv, hkv, d, rank, _dtype_code(V_base), L.stride(0), l_agent_stride, kernel=kernel)
+    _check(lib.lora_value_expand(ctypes.byref(dims), V_base.data_ptr(), L.data_ptr(), B.data_ptr(), N,
+                                 V_out.data_ptr(), _stream_ptr(stream)))
+    return V_out
 
 
 def device_error() -> int:

@@ -22,6 +22,7 @@
 #include "build_tc.cuh"
 #include "prefill_mma.cuh"
 #include "prefill_tc.cuh"
+#include "expand.cuh"
 
 namespace {
 
@@ -354,6 +355,67 @@ fla_status flash_lora_attn_decode_noalloc(const fla_attn_dims *dims, const void 
   }
   return flash_lora_attn_decode(dims, Q, K_base, V_base, L, B, offsets, n_req, total_tokens, O, scratch,
                                 need > 0 ? kNoAllocScratchBytes : 0, stream);
+}
+
+// ---------------------------------------------------------------------------
+fla_status lora_value_expand(const fla_attn_dims *dims, const void *V_base, const void *L, const void *B,
+                             int64_t n_tokens, void *V_out, fla_stream_t stream) {
+  g_last_error.clear();
+  float scale;
+  fla_status st = check_dims(dims, &scale);
+  if (st != FLA_OK) return st;
+  if (n_tokens < 0) return fail(FLA_ERR_INVALID_ARG, "n_tokens must be >= 0");
+  if (!B) return fail(FLA_ERR_INVALID_ARG, "B must be non-NULL");
+  if (n_tokens == 0) return FLA_OK;
+  if (!V_base || !L || !V_out) return fail(FLA_ERR_INVALID_ARG, "V_base, L and V_out must be non-NULL");
+  const fla_attn_dims &d = *dims;
+  if (d.head_dim % 8 != 0)
+    return fail(FLA_ERR_UNSUPPORTED, "lora_value_expand: head_dim %d must be a multiple of 8", d.head_dim);
+  if (!aligned16(V_base) || !aligned16(V_out))
+    return fail(FLA_ERR_INVALID_ARG, "lora_value_expand: V_base and V_out must be 16-byte aligned");
+  if (d.kernel == FLA_KERNEL_TCGEN05)
+    return fail(FLA_ERR_UNSUPPORTED, "lora_value_expand has no tcgen05 kernel (use TENSOR or MMA_SYNC)");
+  const bool mma_shape = d.dtype == FLA_BF16 && (d.head_dim == 64 || d.head_dim == 128) && d.rank % 16 == 0 &&
+                         d.l_row_stride % 2 == 0 && d.l_agent_stride % 2 == 0 &&
+                         (reinterpret_cast<uintptr_t>(L) & 3u) == 0;
+  const bool use_mma = d.kernel != FLA_KERNEL_SIMT && mma_shape;
+  if ((d.kernel == FLA_KERNEL_TENSOR || d.kernel == FLA_KERNEL_MMA_SYNC) && !use_mma)
+    return fail(FLA_ERR_UNSUPPORTED, "lora_value_expand: shape outside the mma.sync kernel (bf16; head_dim 64 or "
+                "128; rank %% 16 == 0; even L strides; 4-byte aligned L)");
+  const int group = fla::expand_agents_per_group(d.n_agents, d.rank, d.head_dim, use_mma);
+  if (group < 1)
+    return fail(FLA_ERR_UNSUPPORTED, "lora_value_expand: rank %d x head_dim %d of B exceeds the %d-byte "
+                "shared-memory budget", d.rank, d.head_dim, fla::kExpMaxSmem);
+  const size_t smem = (size_t)group * d.rank * d.head_dim * (use_mma ? 2 : 4);
+  const int rows = fla::expand_rows_per_cta(n_tokens, d.hkv, fla::device_sm_count());
+  const int64_t tiles = (n_tokens + rows - 1) / rows;
+  if (tiles > 0x7fffffffLL || d.hkv > 65535) return fail(FLA_ERR_UNSUPPORTED, "lora_value_expand: grid too large");
+  fla::ExpandParams p{};
+  p.V = V_base; p.L = L; p.B = B; p.Vout = V_out;
+  p.n_tokens = n_tokens; p.l_row_stride = d.l_row_stride; p.l_agent_stride = d.l_agent_stride;
+  p.A = d.n_agents; p.hkv = d.hkv; p.d = d.head_dim; p.r = d.rank;
+  p.rows_per_cta = rows; p.agents_per_group = group;
+  const dim3 grid((unsigned)tiles, (unsigned)d.hkv);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  auto launch = [&](const void *fn, auto kernel, int threads) {
+    e = fla::ensure_dynamic_smem(fn, (int)smem);
+    if (e == cudaSuccess) kernel<<<grid, threads, smem, s>>>(p);
+  };
+  if (use_mma && d.head_dim == 128)
+    launch(reinterpret_cast<const void *>(fla::lora_value_expand_mma_kernel<128>),
+           fla::lora_value_expand_mma_kernel<128>, fla::kExpMmaWarps * 32);
+  else if (use_mma)
+    launch(reinterpret_cast<const void *>(fla::lora_value_expand_mma_kernel<64>),
+           fla::lora_value_expand_mma_kernel<64>, fla::kExpMmaWarps * 32);
+  else if (d.dtype == FLA_BF16)
+    launch(reinterpret_cast<const void *>(fla::lora_value_expand_kernel<__nv_bfloat16>),
+           fla::lora_value_expand_kernel<__nv_bfloat16>, fla::kExpThreads);
+  else
+    launch(reinterpret_cast<const void *>(fla::lora_value_expand_kernel<float>), fla::lora_value_expand_kernel<float>,
+           fla::kExpThreads);
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "lora_value_expand: %s", cudaGetErrorString(e));
+  return check_launch("lora_value_expand");
 }
 
 }  // extern "C"

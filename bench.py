@@ -488,6 +488,52 @@ def run_legs(args, device, peaks, only=None):
         out[f"{name}/decode"] = {"us": t * 1e6, "queries_per_s": w.n_req * A / t, "gbs": byts / t / 1e9,
                                  "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
         del Q, K, V, L, B, O
+    # ---- baselines on the 8B decode (not the hot path): naive materialisation
+    #      (V_i = V_base + L_i.B_i expanded, then plain attention per agent)
+    #      and non-shared caches (a full K/V cache per agent)
+    base_legs = ("llama8b_decode/lora_value_expand", "llama8b_decode/naive_materialised",
+                 "llama8b_decode/non_shared")
+    if any(want(n) for n in base_legs):
+        from attention_flash_lora_attn_b300 import baselines
+        w = WORKLOADS["llama8b_decode"]
+        N, A, r, hkv, d = w.total_tokens, w.n_agents, w.rank, w.hkv, w.head_dim
+        Q, K, V = rnd((1, A, w.hq, d)), rnd((N, hkv, d)), rnd((N, hkv, d))
+        L, B = rnd((N, A * r)), rnd((A, r, hkv * d), 0.02)
+        offs = torch.tensor([0, N], dtype=torch.int32, device=device)
+        kv = N * hkv * d * 2  # bytes of one K or V cache
+        expand_bytes = kv + N * A * r * 2 + A * r * hkv * d * 2 + A * kv  # V_base, L, B in; A x V_i out
+        plain_bytes = 2 * kv + N * baselines.ZERO_RANK * 2                # one agent's K, V (+ zero LR cache)
+        fused = out.get("llama8b_decode/decode", {}).get("us")
+        if want("llama8b_decode/lora_value_expand") or want("llama8b_decode/naive_materialised"):
+            naive = baselines.PreparedBaselineDecode("naive", Q, offs, K_base=K, V_base=V, L=L, B=B, rank=r,
+                                                     stream=stream)
+            if want("llama8b_decode/lora_value_expand"):
+                t = _median_launch_s(naive.expand, reps, stream, flush)
+                out["llama8b_decode/lora_value_expand"] = {
+                    "us": t * 1e6, "bytes": expand_bytes, "gbs": expand_bytes / t / 1e9,
+                    "hbm_frac": expand_bytes / t / 1e9 / peaks["hbm_gbs"]}
+            if want("llama8b_decode/naive_materialised"):
+                t = _median_launch_s(naive, reps, stream, flush)
+                byts = expand_bytes + A * plain_bytes
+                leg = {"us": t * 1e6, "queries_per_s": A / t, "bytes": byts, "gbs": byts / t / 1e9,
+                       "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
+                if fused:
+                    leg["time_vs_fused_decode"] = t * 1e6 / fused
+                out["llama8b_decode/naive_materialised"] = leg
+            del naive
+        if want("llama8b_decode/non_shared"):
+            Ks = [rnd((N, hkv, d)) for _ in range(A)]
+            Vs = [rnd((N, hkv, d)) for _ in range(A)]
+            ns = baselines.PreparedBaselineDecode("non_shared", Q, offs, K=Ks, V=Vs, stream=stream)
+            t = _median_launch_s(ns, reps, stream, flush)
+            byts = A * plain_bytes
+            leg = {"us": t * 1e6, "queries_per_s": A / t, "bytes": byts, "cache_bytes": A * 2 * kv,
+                   "gbs": byts / t / 1e9, "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
+            if fused:
+                leg["time_vs_fused_decode"] = t * 1e6 / fused
+            out["llama8b_decode/non_shared"] = leg
+            del ns, Ks, Vs
+        del Q, K, V, L, B
     # ---- full LR-cache build, 131072 x 8192 . 8192 x 320
     w = WORKLOADS["llama70b_decode"]
     # the first 16384 rows of the 70B build: a profiler-sized case of the same kernel

@@ -219,6 +219,36 @@ FLA_API fla_status flash_lora_attn_decode_noalloc(const fla_attn_dims *dims, con
                                                   const int32_t *offsets, int32_t n_req, int64_t total_tokens,
                                                   float *O, fla_stream_t stream);
 
+/*
+ * lora_value_expand - the materialised value cache of every agent:
+ *   V_out[a, t, h, :] = V_base[t, h, :] + L[t, a*l_agent_stride + (0..r-1)] . B[a, :, h*d:(h+1)*d]
+ *
+ * LRAgent summary, Metodologia section 1 (V_i = V_base + L_i.B_i) and section
+ * 3, Problema bullet: this full-width reconstruction for every agent is what
+ * Flash-LoRA-Attention avoids.  It is provided as the first half of the
+ * naive-materialisation baseline (plain attention over each V_i is the
+ * second) that the reordered decode is measured against.  No decode or
+ * prefill call uses it.
+ *
+ *   V_base  [n_tokens, hkv, d]                 (input)
+ *   L       [n_tokens, l_row_stride]           (input)
+ *   B       [A, r, hkv*d]                      (input)
+ *   V_out   [A, n_tokens, hkv, d], same dtype  (output; agent-major)
+ * Uses n_agents, hkv, head_dim, rank, dtype, l_row_stride, l_agent_stride and
+ * kernel of `dims` (hq and softmax_scale are validated as for decode but not
+ * used).  fp32 accumulation, one rounding to the storage dtype per value.
+ * Kernels: mma.sync (bf16; head_dim 64 or 128; rank % 16 == 0; even
+ * l_row_stride and l_agent_stride; L 4-byte aligned; rank x head_dim x 2
+ * bytes at most 96 KiB); CUDA cores otherwise (head_dim % 8 == 0; rank x
+ * head_dim x 4 bytes at most 96 KiB).  TCGEN05 is UNSUPPORTED.  V_base and
+ * V_out must be 16-byte aligned.
+ * Errors: INVALID_ARG (null pointer with n_tokens > 0, n_tokens < 0,
+ * alignment, the dims checks of decode), UNSUPPORTED (shape outside the
+ * selected kernel), CUDA (launch failure).  n_tokens == 0 is a no-op.
+ */
+FLA_API fla_status lora_value_expand(const fla_attn_dims *dims, const void *V_base, const void *L, const void *B,
+                                     int64_t n_tokens, void *V_out, fla_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 FLA_API const char *fla_status_string(fla_status status);
 

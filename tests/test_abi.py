@@ -132,3 +132,21 @@ def test_valid_call_without_gpu_reports_cuda_error(lib):
     p = ctypes.c_void_p(16)
     st = lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 1, 1, None)
     assert st == 4
+
+
+def test_value_expand_validates_on_the_host(lib):
+    p, odd = ctypes.c_void_p(16), ctypes.c_void_p(8)
+    d = _dims()
+    assert lib.lora_value_expand(ctypes.byref(d), p, p, p, 0, p, None) == 0       # empty: no-op
+    assert lib.lora_value_expand(ctypes.byref(d), p, p, p, -1, p, None) == 1      # n_tokens < 0
+    assert lib.lora_value_expand(ctypes.byref(d), None, p, p, 8, p, None) == 1    # V_base NULL
+    assert lib.lora_value_expand(ctypes.byref(d), p, p, p, 8, odd, None) == 1     # V_out misaligned
+    assert lib.lora_value_expand(ctypes.byref(_dims(hq=30)), p, p, p, 8, p, None) == 1
+    d12 = _dims(hq=8, hkv=8, head_dim=12)
+    assert lib.lora_value_expand(ctypes.byref(d12), p, p, p, 8, p, None) == 2     # head_dim % 8
+    big = _dims(head_dim=256, rank=256, l_row_stride=768, l_agent_stride=256)
+    big.dtype = 0                                                                  # fp32: the CUDA-core kernel
+    assert lib.lora_value_expand(ctypes.byref(big), p, p, p, 8, p, None) == 2     # shared memory
+    d5 = _dims()
+    d5.kernel = 4
+    assert lib.lora_value_expand(ctypes.byref(d5), p, p, p, 8, p, None) == 2      # no tcgen05 kernel
