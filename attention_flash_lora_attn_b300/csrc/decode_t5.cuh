@@ -18,13 +18,17 @@
 //   O^T += V_tile^T . P^T      M = d = 128, K = keys: V as an MN-major A
 //   OL^T+= L_tile^T . P^T      M = 128 L columns per MMA (every agent's r
 //                              columns), so the TMEM cost per row is 1 column
-//   l   += 1^T . P^T           row sums from an all-ones A operand
+//   l                          row sums: each softmax thread adds its key's P
+//                              values into its own TMEM lane (64 columns, one
+//                              per query row); the 128 lanes are summed once,
+//                              after the last tile
 // P^T (bf16, key-major rows of 64 query rows) is written by the four softmax
 // warps to shared memory as an MN-major B operand.  The running max per query
 // row lives in shared memory; exponentials use it speculatively and the CTA
 // votes once per tile on whether any row's max rose by more than 2^8, in which
 // case (rarely, and on the first tile) the row maxima are reduced across the
-// 128 keys, O^T, OL^T and l are rescaled in TMEM and P is recomputed.
+// 128 keys, O^T, OL^T and the per-lane row sums are rescaled in TMEM and P
+// is recomputed.
 //
 // Warp roles: warp 0 lane 0 streams the K ring (128-token tiles), warp 6
 // lane 0 the V|L ring (64-token halves); warp 1 owns TMEM and lane 0 issues
@@ -55,7 +59,6 @@ constexpr uint32_t kColS0 = 0, kColS1 = 64, kColO = 128, kColLs = 192, kColOL = 
 constexpr float kRescaleLog2 = 8.f;
 constexpr int kQBytes = kN * D * 2;        // 16 KB
 constexpr int kPBytes = kKeys * kN * 2;    // 16 KB
-constexpr int kOnesBytes = 1024;
 constexpr int kKBytes = kKeys * D * 2;     // 32 KB
 constexpr int kVBytes = kHalf * D * 2;     // 16 KB
 constexpr int kLBoxBytes = kHalf * 128;    // one 64-column L box of a half tile
@@ -76,12 +79,6 @@ __device__ __forceinline__ bool wait_ab(uint32_t bar, uint32_t parity, volatile 
   return ptx::mbar_wait_or_abort(bar, parity, abort_flag, kErrDecodeT5Wait);
 }
 
-// All-ones A operand: one 8-row swizzle atom and a zero stride between row
-// groups, so every row of the M = 128 operand reads the same ones.
-__device__ __forceinline__ uint64_t desc_ones(uint32_t saddr) {
-  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmL, const Params p) {
@@ -89,8 +86,7 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *q_s = smem;
   uint8_t *p_s = q_s + kQBytes;
-  uint8_t *ones_s = p_s + kPBytes;
-  uint8_t *k_s = ones_s + kOnesBytes;
+  uint8_t *k_s = p_s + kPBytes;
   uint8_t *vl_s = k_s + p.nk * kKBytes;
   __shared__ __align__(8) uint64_t bars[4 * kMaxRing + 10];
   __shared__ uint32_t s_tmem;
@@ -167,7 +163,7 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     ptx::tmem_alloc(ptx::smem_u32(&s_tmem), 512);
     ptx::tmem_relinquish();
   }
-  // Q rows (n = a*G + g) into the K-major 128-byte-swizzled layout; ones
+  // Q rows (n = a*G + g) into the K-major 128-byte-swizzled layout
   for (int e = threadIdx.x; e < kN * (D / 8); e += kThreads) {
     const int row = e / (D / 8), c8 = e % (D / 8);
     uint4 v = make_uint4(0, 0, 0, 0);
@@ -178,8 +174,6 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     *reinterpret_cast<uint4 *>(q_s + (c8 >> 3) * (kN * 128) + row * 128 + (((c8 & 7) ^ (row & 7)) << 4)) = v;
   }
   if (threadIdx.x < kN) s_m[0][threadIdx.x] = threadIdx.x < p.rows ? -INFINITY : 0.f;
-  for (int e = threadIdx.x; e < kOnesBytes / 16; e += kThreads)
-    reinterpret_cast<uint4 *>(ones_s)[e] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
   ptx::fence_proxy_async_smem();
   ptx::tc_fence_before();
   __syncthreads();
@@ -239,12 +233,10 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) {
       const uint32_t idesc_s = ptx::idesc_bf16_f32(kKeys, kN);                           // K, Q: K-major
       const uint32_t idesc_v = ptx::idesc_bf16_f32(kKeys, kN) | (1u << 15) | (1u << 16);  // V/L and P: MN-major
-      const uint32_t idesc_1 = ptx::idesc_bf16_f32(kKeys, kN) | (1u << 16);              // ones K-major, P MN-major
       const uint64_t d_q = ptx::smem_desc_k128(ptx::smem_u32(q_s));
       const uint64_t d_k = ptx::smem_desc_k128(ptx::smem_u32(k_s));
       const uint64_t d_p = ptx::smem_desc_mn128(ptx::smem_u32(p_s), 8192);
       const uint64_t d_vl = ptx::smem_desc_mn128(ptx::smem_u32(vl_s), kLBoxBytes);
-      const uint64_t d_ones = desc_ones(ptx::smem_u32(ones_s));
       auto issue_s = [&](int j) -> bool {
         const int st = j % p.nk, b = j & 1;
         if (!wait_ab(kf(st), (j / p.nk) & 1, &s_abort)) return false;
@@ -278,7 +270,6 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             for (int c = 0; c < p.n_lchunk; ++c)
               ptx::tc_mma_f16(tmem + kColOL + c * kN, ptx::desc_advance(dl, c * 2 * kLBoxBytes + ks * 2048), bP,
                               idesc_v, acc);
-            ptx::tc_mma_f16(tmem + kColLs, d_ones, bP, idesc_1, acc);
           }
           ptx::tc_commit(ve(st));
         }
@@ -424,9 +415,57 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(pfull);
+      // row sums of this key's lane: the same bf16 P values the MMAs use
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t lv[32];
+        if (j > 0) {
+          ptx::tmem_ld32(tmem + lane_base + kColLs + hh * 32, lv);
+          ptx::tmem_ld_wait();
+          ptx::reg_fence32(lv);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t w = pk[hh * 16 + i];
+          const float p0 = __uint_as_float(w << 16), p1 = __uint_as_float(w & 0xFFFF0000u);
+          lv[2 * i] = __float_as_uint(j > 0 ? __uint_as_float(lv[2 * i]) + p0 : p0);
+          lv[2 * i + 1] = __float_as_uint(j > 0 ? __uint_as_float(lv[2 * i + 1]) + p1 : p1);
+        }
+        ptx::tmem_st32(tmem + lane_base + kColLs + hh * 32, lv);
+      }
+      ptx::tmem_st_wait();
     }
     // ---- partial record: [rows][d + r] (O | own agent's OL) | m[rows] | l[rows]
     if (ok && n > 0) ok = __all_sync(0xffffffffu, wait_ab(pvdone, (n - 1) & 1, &s_abort));
+    // row sums: reduce-scatter each warp's 32 lanes (lane L ends with rows 2L,
+    // 2L+1), then add the four warps' shares through the P buffer, which the
+    // completed last P.V MMAs no longer read.  Every softmax warp reaches the
+    // named barrier once, whatever its ok.
+    float *lred = reinterpret_cast<float *>(p_s);  // [4 warps][64 rows]
+    if (ok && n > 0) {
+      uint32_t lw[kN];
+      ptx::tmem_ld32(tmem + lane_base + kColLs, *reinterpret_cast<uint32_t(*)[32]>(&lw[0]));
+      ptx::tmem_ld32(tmem + lane_base + kColLs + 32, *reinterpret_cast<uint32_t(*)[32]>(&lw[32]));
+      ptx::tmem_ld_wait();
+      ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&lw[0]));
+      ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&lw[32]));
+      float lv[kN];
+#pragma unroll
+      for (int c = 0; c < kN; ++c) lv[c] = __uint_as_float(lw[c]);
+#pragma unroll
+      for (int o = 16, nh = kN / 2; o >= 1; o >>= 1, nh >>= 1) {
+        const bool upper = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < nh; ++i) {
+          const float send = upper ? lv[i] : lv[i + nh];
+          const float keep = upper ? lv[i + nh] : lv[i];
+          lv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      }
+      lred[q * kN + 2 * lane] = lv[0];
+      lred[q * kN + 2 * lane + 1] = lv[1];
+    }
+    asm volatile("bar.sync 1, 128;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (unit == 0 && key == 0) p.pair_info[qreq * p.hkv + head] = make_int2(slot - unit, n_units);
     if (ok) {
@@ -459,18 +498,9 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             }
           }
         }
-        ptx::tmem_ld32(tmem + lane_base + kColLs, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-        ptx::tmem_ld32(tmem + lane_base + kColLs + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
-        ptx::tmem_ld_wait();
-        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-        ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
-        if (key == 0) {
-#pragma unroll
-          for (int c = 0; c < kN; ++c)
-            if (c < p.rows) {
-              part[p.rows * W + c] = s_m[n_resc & 1][c];
-              part[p.rows * W + p.rows + c] = __uint_as_float(ov[c]);
-            }
+        if (key < p.rows) {
+          part[p.rows * W + key] = s_m[n_resc & 1][key];
+          part[p.rows * W + p.rows + key] = (lred[key] + lred[kN + key]) + (lred[2 * kN + key] + lred[3 * kN + key]);
         }
       } else {
         // empty unit (an empty request): zero accumulators, m = -inf, l = 0
@@ -521,7 +551,7 @@ inline DecodeT5Plan decode_t5_plan(const fla_attn_dims &d) {
   const int vl_bytes = dt5::kVBytes + n_lbox * dt5::kLBoxBytes;
   const int spare = (n_lbox & 1) ? dt5::kLBoxBytes : 0;
   const int budget = 227 * 1024 - 1024 /* alignment */ - 3072 /* static shared */;
-  const int fixed = dt5::kQBytes + dt5::kPBytes + dt5::kOnesBytes;
+  const int fixed = dt5::kQBytes + dt5::kPBytes;
   int nk = 2, nv = (budget - fixed - nk * dt5::kKBytes - spare) / vl_bytes;
   if (nv > 6) nv = 6;
   if (nv < 2) return pl;
