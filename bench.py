@@ -56,14 +56,19 @@ def load_peaks():
         return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
 
 
-def kernel_source_hash() -> str:
-    """Hash of the CUDA sources; a stored ncu traffic figure is used only while it matches."""
+# Sources the headline decode kernels (decode_tc_kernel and its merge kernels)
+# are compiled from: their own header and the helpers it includes.
+HEADLINE_KERNEL_SOURCES = ("decode_tc.cuh", "ptx.cuh", "fla_common.cuh")
+
+
+def kernel_source_hash(files=HEADLINE_KERNEL_SOURCES) -> str:
+    """Hash of the headline kernels' CUDA sources; a stored ncu traffic figure
+    is used only while it matches (an edit to another kernel leaves it valid)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_flash_lora_attn_b300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, fn), "rb") as f:
-                h.update(fn.encode() + f.read())
+    for fn in sorted(files):
+        with open(os.path.join(csrc, fn), "rb") as f:
+            h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
 
 
