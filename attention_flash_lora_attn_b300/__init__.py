@@ -5,6 +5,7 @@ Public API (thin wrappers over the C ABI in include/flash_lora_attn.h):
   flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, rank=...)
   flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0, rank=...)
   PreparedDecode(...)                       a decode call marshalled once, one C call per step
+  PreparedDecodeHostIO(...)                 the same with host Q in / host O out in that one call
   lora_value_expand(V_base, L, B, rank=...) every agent's V_i = V_base + L_i.B_i (baseline only)
   device_error()                            read and clear the device error word
 
@@ -19,6 +20,7 @@ from .binding import (  # noqa: F401
     LIB_PATH,
     FlaError,
     PreparedDecode,
+    PreparedDecodeHostIO,
     device_error,
     flash_lora_attn_decode,
     flash_lora_attn_prefill,

@@ -28,7 +28,7 @@ STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "F
 EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
             "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
             "fla_last_error_message", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc",
-            "lora_value_expand")
+            "lora_value_expand", "flash_lora_attn_decode_host_io")
 
 
 class FlaError(RuntimeError):
@@ -82,6 +82,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flash_lora_attn_decode_noalloc.restype = ctypes.c_int
         lib.lora_value_expand.argtypes = [dims_p, vp, vp, vp, i64, vp, vp]
         lib.lora_value_expand.restype = ctypes.c_int
+        lib.flash_lora_attn_decode_host_io.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp,
+                                                       sz, vp]
+        lib.flash_lora_attn_decode_host_io.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -245,6 +248,57 @@ class PreparedDecode:
         if st != FLA_OK:
             _check(st)
         return self.O
+
+
+class PreparedDecodeHostIO:
+    """A host-buffer decode marshalled once (flash_lora_attn_decode_host_io).
+
+    Each call enqueues the copy Q_host -> Q_dev, the decode into O_dev and the
+    copy O_dev -> O_host with one C call.  Q_host and O_host are CPU tensors
+    (pin them for asynchronous copies); O_host is valid once the stream has
+    passed the call.  Other arguments as for flash_lora_attn_decode.
+    """
+
+    def __init__(self, Q_host, Q_dev, K_base, V_base, L, B, offsets, *, rank: int, O_dev, O_host,
+                 l_agent_stride: Optional[int] = None, scale: Optional[float] = None,
+                 workspace: Optional[torch.Tensor] = None, kernel: str = "auto", stream=None):
+        lib = load_library()
+        _need_cuda(Q_dev, K_base, V_base, L, B, offsets, O_dev, workspace)
+        if Q_host.is_cuda or O_host.is_cuda:
+            raise ValueError("Q_host and O_host must be host (CPU) tensors")
+        for t, nm in ((Q_host, "Q_host"), (Q_dev, "Q_dev"), (K_base, "K_base"), (V_base, "V_base"), (B, "B"),
+                      (O_dev, "O_dev"), (O_host, "O_host")):
+            _dense(t, nm)
+        if Q_host.shape != Q_dev.shape or Q_host.dtype != Q_dev.dtype:
+            raise ValueError("Q_host and Q_dev must have the same shape and dtype")
+        R, A, hq, d = Q_dev.shape
+        if tuple(O_dev.shape) != (R, A, hq, d) or O_dev.dtype != torch.float32 or O_host.shape != O_dev.shape \
+                or O_host.dtype != torch.float32:
+            raise ValueError("O_dev and O_host must be fp32 [R, A, Hq, d]")
+        if L.stride(1) != 1:
+            raise ValueError("L must have unit column stride")
+        N, hkv, _ = K_base.shape
+        if l_agent_stride is None:
+            l_agent_stride = rank
+        self.dims = make_dims(A, hq, hkv, d, rank, _dtype_code(Q_dev), L.stride(0), l_agent_stride, scale, kernel)
+        sp = _stream_ptr(stream)
+        need = lib.flash_lora_attn_decode_workspace_size(ctypes.byref(self.dims), R, N)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=Q_dev.device)
+        self.O_host = O_host
+        self._keep = (Q_host, Q_dev, K_base, V_base, L, B, offsets, O_dev, O_host, workspace)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+        self._fn = lib.flash_lora_attn_decode_host_io
+        self._args = (ctypes.byref(self.dims), Q_host.data_ptr(), Q_dev.data_ptr(), K_base.data_ptr(),
+                      V_base.data_ptr(), L.data_ptr(), B.data_ptr(), offsets.data_ptr(), R, N, O_dev.data_ptr(),
+                      O_host.data_ptr(), ws_ptr, ws_bytes, sp)
+
+    def __call__(self) -> torch.Tensor:
+        st = self._fn(*self._args)
+        if st != FLA_OK:
+            _check(st)
+        return self.O_host
 
 
 def flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0: int, *, rank: int,

@@ -418,4 +418,34 @@ fla_status lora_value_expand(const fla_attn_dims *dims, const void *V_base, cons
   return check_launch("lora_value_expand");
 }
 
+// ---------------------------------------------------------------------------
+fla_status flash_lora_attn_decode_host_io(const fla_attn_dims *dims, const void *Q_host, void *Q_dev,
+                                          const void *K_base, const void *V_base, const void *L, const void *B,
+                                          const int32_t *offsets, int32_t n_req, int64_t total_tokens,
+                                          float *O_dev, float *O_host, void *workspace, size_t workspace_bytes,
+                                          fla_stream_t stream) {
+  g_last_error.clear();
+  if (!dims) return fail(FLA_ERR_INVALID_ARG, "dims is NULL");
+  if (!Q_host || !Q_dev || !O_dev || !O_host)
+    return fail(FLA_ERR_INVALID_ARG, "Q_host, Q_dev, O_dev and O_host must be non-NULL");
+  if (n_req < 0) return fail(FLA_ERR_INVALID_ARG, "n_req must be >= 0");
+  const size_t esize = dims->dtype == FLA_BF16 ? 2 : 4;
+  const size_t elems = (size_t)n_req * dims->n_agents * dims->hq * dims->head_dim;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // the shape checks shared with decode run before the copy; the decode's own
+  // remaining checks run after it (documented: Q_dev may then hold the queries)
+  float scale;
+  fla_status st = check_dims(dims, &scale);
+  if (st != FLA_OK) return st;
+  if (elems == 0) return FLA_OK;
+  cudaError_t e = cudaMemcpyAsync(Q_dev, Q_host, elems * esize, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "decode_host_io: copying Q to the device: %s", cudaGetErrorString(e));
+  st = flash_lora_attn_decode(dims, Q_dev, K_base, V_base, L, B, offsets, n_req, total_tokens, O_dev, workspace,
+                              workspace_bytes, stream);
+  if (st != FLA_OK) return st;
+  e = cudaMemcpyAsync(O_host, O_dev, elems * sizeof(float), cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "decode_host_io: copying O to the host: %s", cudaGetErrorString(e));
+  return FLA_OK;
+}
+
 }  // extern "C"

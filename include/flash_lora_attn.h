@@ -249,6 +249,33 @@ FLA_API fla_status flash_lora_attn_decode_noalloc(const fla_attn_dims *dims, con
 FLA_API fla_status lora_value_expand(const fla_attn_dims *dims, const void *V_base, const void *L, const void *B,
                                      int64_t n_tokens, void *V_out, fla_stream_t stream);
 
+/*
+ * flash_lora_attn_decode_host_io - flash_lora_attn_decode for queries that
+ * arrive in host memory and outputs that are wanted there: one call enqueues,
+ * on `stream`, the copy Q_host -> Q_dev, the decode of Q_dev into O_dev and
+ * the copy O_dev -> O_host.  A serving loop's step is then one library call.
+ * The pages have no counterpart: this is a library convenience.
+ *
+ *   Q_host   host [n_req, A, hq, d] in dims->dtype; page-locked (pinned)
+ *            memory keeps both copies asynchronous
+ *   Q_dev    device buffer of the same size (the decode's Q)
+ *   O_dev    device fp32 [n_req, A, hq, d] (the decode's O)
+ *   O_host   host fp32 [n_req, A, hq, d], pinned as above; valid once the
+ *            stream has reached the end of this call's work
+ *   the other arguments as for flash_lora_attn_decode.
+ * Allocates nothing; the copies are plain cudaMemcpyAsync calls.  The shape
+ * checks shared with decode run before anything is enqueued; when a later
+ * decode check fails, the Q copy has been enqueued (Q_dev is overwritten) but
+ * no kernel is launched.  n_req == 0 is a no-op.
+ * Errors: as for flash_lora_attn_decode, plus INVALID_ARG for a NULL host or
+ * staging pointer and CUDA when a copy cannot be enqueued.
+ */
+FLA_API fla_status flash_lora_attn_decode_host_io(const fla_attn_dims *dims, const void *Q_host, void *Q_dev,
+                                                  const void *K_base, const void *V_base, const void *L,
+                                                  const void *B, const int32_t *offsets, int32_t n_req,
+                                                  int64_t total_tokens, float *O_dev, float *O_host, void *workspace,
+                                                  size_t workspace_bytes, fla_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 FLA_API const char *fla_status_string(fla_status status);
 

@@ -150,3 +150,18 @@ def test_value_expand_validates_on_the_host(lib):
     d5 = _dims()
     d5.kernel = 4
     assert lib.lora_value_expand(ctypes.byref(d5), p, p, p, 8, p, None) == 2      # no tcgen05 kernel
+
+
+def test_decode_host_io_validates_on_the_host(lib):
+    p = ctypes.c_void_p(16)
+    d = _dims()
+
+    def call(qh=p, qd=p, od=p, oh=p, n_req=1, dims=d):
+        return lib.flash_lora_attn_decode_host_io(ctypes.byref(dims), qh, qd, p, p, p, p, p, n_req, 16, od, oh,
+                                                  None, 0, None)
+    assert call(qh=None) == 1
+    assert call(oh=None) == 1
+    assert call(qd=None) == 1
+    assert call(n_req=-1) == 1
+    assert call(dims=_dims(hq=30)) == 1     # a decode shape check, before anything is enqueued
+    assert call(n_req=0) == 0               # no queries: no-op

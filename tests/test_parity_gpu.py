@@ -193,6 +193,29 @@ def test_prepared_decode_matches_the_function():
         assert torch.equal(O1, O2)
 
 
+def test_decode_host_io_matches_the_device_decode():
+    """One host-buffer call (copy in, decode, copy out) gives the device decode's output, twice in a row."""
+    fla = _fla()
+    w = small_workload(3, 32, 8, 128, 16)
+    x = make_decode_inputs(w, seed=31, lengths=[1500, 7])
+    d = to_dev(x)
+    Qh = x["Q"].clone().pin_memory()
+    Qd = torch.empty_like(d["Q"])
+    Od = torch.empty(d["Q"].shape, dtype=torch.float32, device="cuda")
+    Oh = torch.empty(d["Q"].shape, dtype=torch.float32).pin_memory()
+    call = fla.PreparedDecodeHostIO(Qh, Qd, d["K_base"], d["V_base"], d["L"], d["B"], d["offsets"], rank=16,
+                                    O_dev=Od, O_host=Oh)
+    for step in range(2):
+        if step:
+            Qh.copy_(make_decode_inputs(w, seed=37, lengths=[1500, 7])["Q"])
+        call()
+        torch.cuda.synchronize()
+        want = fla.flash_lora_attn_decode(Qh.cuda(), d["K_base"], d["V_base"], d["L"], d["B"], d["offsets"], rank=16)
+        assert torch.equal(Oh, want.cpu()), f"step {step}"
+    ref = oracle.decode(Qh, x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"].numpy(), rank=16)
+    check_attn(Oh, ref, what="host io")
+
+
 def test_decode_output_guard_bands():
     """Writes stay inside O: canaries around the output are untouched."""
     w = small_workload(3, 32, 8, 128, 16)
