@@ -268,3 +268,27 @@ def test_ragged_lengths_recipe():
     w = WORKLOADS["llama8b_ragged"]
     assert w.n_req == 32 and w.total_tokens == 614602
     assert min(w.lengths) == 4174 and max(w.lengths) == 31930
+
+
+def test_agent_value_cache_by_brute_force():
+    """V_i[t, h, j] = V_base[t, h, j] + sum_k L_i[t, k] B_i[k, h*d + j], element by element
+    (LRAgent summary, Metodologia section 1).  Integer inputs make every product exact,
+    so a transposed head slice or a dropped term shows as a mismatch."""
+    rng = np.random.default_rng(5)
+    n, hkv, d, r = 3, 2, 4, 3
+    V = rng.integers(-3, 4, size=(n, hkv, d)).astype(np.float64)
+    L = rng.integers(-2, 3, size=(n, r)).astype(np.float64)
+    B = rng.integers(-2, 3, size=(r, hkv * d)).astype(np.float64)
+    got = oracle.agent_value_cache(V, L, B, hkv, d)
+    assert got.shape == (n, hkv, d)
+    for t in range(n):
+        for h in range(hkv):
+            for j in range(d):
+                want = V[t, h, j] + sum(L[t, k] * B[k, h * d + j] for k in range(r))
+                assert got[t, h, j] == want
+    # B = 0 leaves the base cache; a one-hot L row picks one row of B, split by head
+    assert np.array_equal(oracle.agent_value_cache(V, L, np.zeros_like(B), hkv, d), V)
+    one_hot = np.zeros((n, r))
+    one_hot[:, 1] = 1.0
+    picked = oracle.agent_value_cache(np.zeros_like(V), one_hot, B, hkv, d)
+    assert np.array_equal(picked[0], B[1].reshape(hkv, d))
