@@ -6,14 +6,18 @@ Headline workload (one GPU): the Llama-3-8B-shaped single-layer decode -
 3 agents, 32 query / 8 kv heads, head_dim 128, r 16, shared context 16384
 tokens, one query token per agent, bf16 storage, fp32 accumulation.
 One step = one flash_lora_attn_decode call (scores, online softmax, P.V_base,
-P.L_i, split merge and the B_i epilogue: one kernel).
+P.L_i in the decode kernel; split merge and the B_i epilogue in the merge
+kernel behind it).
 
 Timing: W warm-up steps, then K steps replayed from a CUDA graph between a
 barrier + synchronize on both sides, timed with CUDA events on the launching
-stream.  The step inputs rotate over enough copies of the cache (> 4x the
-126 MB L2) that no step finds its K/V/L tiles in L2.  `e2e` re-times K steps
-through the public Python API with pinned host buffers: each step copies the
-queries host->device, decodes, and reads O back device->host.
+stream, right after 0.25 s of untimed replays (load clocks).  The step inputs
+rotate over enough copies of the cache (> 4x the 126 MB L2) that no step finds
+its K/V/L tiles in L2.  `e2e` re-times K steps through the C-ABI call with host
+buffers (flash_lora_attn_decode_host_io): each step copies the queries from
+pinned host memory to the device, decodes, and copies O back to pinned host
+memory.  The other legs time each remaining hot-path row alone, plus the
+naive-materialisation and non-shared-cache baselines on the headline workload.
 
 Under torchrun each rank runs its own independent copy of the workload
 (weak scaling, no collective on the data path); value = all ranks' queries
