@@ -15,7 +15,9 @@
  *
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers to caller-owned memory on the
- *     current CUDA device; the library never allocates, frees or keeps them.
+ *     current CUDA device (the one exception: the Q_host / O_host buffers of
+ *     flash_lora_attn_decode_host_io); the library never allocates, frees or
+ *     keeps them.
  *   - Tensors are dense row-major unless a stride argument says otherwise.
  *   - Calls are enqueued on `stream` (NULL = the legacy default stream), are
  *     asynchronous and never synchronise the host.
