@@ -1,7 +1,7 @@
 """Flash-LoRA-Attention for B300 (sm_103a).
 
 Public API (thin wrappers over the C ABI in include/flash_lora_attn.h):
-  lr_cache_build(X, A_t, L=None)            L = X . A_cat for every agent at once
+  lr_cache_build(X, A_cat, L=None)          L = X . A_cat for every agent at once
   flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, rank=...)
   flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0, rank=...)
   PreparedDecode(...)                       a decode call marshalled once, one C call per step

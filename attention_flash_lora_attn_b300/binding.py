@@ -27,7 +27,7 @@ STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "F
 # Every symbol the header declares (tests check that the library exports them).
 EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
             "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
-            "fla_last_error_message", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc",
+            "fla_last_error", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc",
             "lora_value_expand", "flash_lora_attn_decode_host_io")
 
 
@@ -60,7 +60,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib = ctypes.CDLL(path)
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         dims_p = ctypes.POINTER(AttnDims)
-        lib.lr_cache_build.argtypes = [vp, i64, vp, vp, i64, i64, i32, i32, i32, i32, vp]
+        lib.lr_cache_build.argtypes = [vp, i64, vp, vp, i64, i64, i32, i32, i32, i32, i32, vp]
         lib.lr_cache_build.restype = ctypes.c_int
         lib.flash_lora_attn_decode_workspace_size.argtypes = [dims_p, i32, i64]
         lib.flash_lora_attn_decode_workspace_size.restype = sz
@@ -72,8 +72,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flash_lora_attn_prefill.restype = ctypes.c_int
         lib.fla_status_string.argtypes = [ctypes.c_int]
         lib.fla_status_string.restype = ctypes.c_char_p
-        lib.fla_last_error_message.argtypes = []
-        lib.fla_last_error_message.restype = ctypes.c_char_p
+        lib.fla_last_error.argtypes = []
+        lib.fla_last_error.restype = ctypes.c_char_p
         lib.fla_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
         lib.fla_device_error.restype = ctypes.c_int
         lib.fla_version.argtypes = []
@@ -91,7 +91,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def _check(status: int):
     if status != FLA_OK:
-        msg = load_library().fla_last_error_message().decode(errors="replace")
+        msg = load_library().fla_last_error().decode(errors="replace")
         raise FlaError(status, msg)
 
 
@@ -139,28 +139,34 @@ def make_dims(n_agents, hq, hkv, head_dim, rank, dtype_code, l_row_stride, l_age
                     0.0 if scale is None else float(scale), KERNELS[kernel])
 
 
-def lr_cache_build(X: torch.Tensor, A_t: torch.Tensor, L: Optional[torch.Tensor] = None, *,
-                   kernel: str = "auto", stream=None) -> torch.Tensor:
-    """L = X . A_t^T for every agent at once (A_t = stacked [A*r, D] down-projections).
+def lr_cache_build(X: torch.Tensor, A_cat: torch.Tensor, L: Optional[torch.Tensor] = None, *,
+                   n_agents: int = 1, kernel: str = "auto", stream=None) -> torch.Tensor:
+    """L = X . A_cat for every agent at once (A_cat = [A_1 | ... | A_A], [D, A*r]).
 
-    X [n, D] (rows may be strided), A_t [A*r, D] contiguous, L [n, A*r] (rows
-    may be strided; a column slice of a wider tensor is allowed).
+    X [n, D] (rows may be strided), A_cat [D, A*r] contiguous, L [n, A*r]
+    (rows may be strided; a column slice of a wider tensor is allowed).
+    `n_agents` splits the A*r columns into agents' blocks of rank A*r/n_agents
+    (the product is the same; it only names the blocks at the C ABI).
     """
     lib = load_library()
-    _need_cuda(X, A_t, L)
+    _need_cuda(X, A_cat, L)
     n, D = X.shape
-    N, D2 = A_t.shape
+    D2, N = A_cat.shape
     if D2 != D:
-        raise ValueError("A_t must be [n_cols, d_model]")
+        raise ValueError("A_cat must be [d_model, n_agents * rank]")
+    if n_agents < 1 or N % n_agents != 0:
+        raise ValueError("the A_cat columns must split evenly into n_agents blocks")
     if L is None:
         L = torch.empty((n, N), dtype=X.dtype, device=X.device)
     if X.stride(1) != 1 or L.stride(1) != 1:
         raise ValueError("X and L must have unit column stride")
-    _dense(A_t, "A_t")
-    if not (X.dtype == A_t.dtype == L.dtype):
-        raise TypeError("X, A_t and L must share one dtype")
-    _check(lib.lr_cache_build(X.data_ptr(), X.stride(0), A_t.data_ptr(), L.data_ptr(), L.stride(0), n, D, N,
-                              _dtype_code(X), KERNELS[kernel], _stream_ptr(stream)))
+    if tuple(L.shape) != (n, N):
+        raise ValueError("L must be [n_tokens, n_agents * rank]")
+    _dense(A_cat, "A_cat")
+    if not (X.dtype == A_cat.dtype == L.dtype):
+        raise TypeError("X, A_cat and L must share one dtype")
+    _check(lib.lr_cache_build(X.data_ptr(), X.stride(0), A_cat.data_ptr(), L.data_ptr(), L.stride(0), n, D,
+                              n_agents, N // n_agents, _dtype_code(X), KERNELS[kernel], _stream_ptr(stream)))
     return L
 
 

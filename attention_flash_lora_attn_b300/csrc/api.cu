@@ -98,7 +98,7 @@ const char *fla_status_string(fla_status s) {
   return "FLA_ERR_UNKNOWN";
 }
 
-const char *fla_last_error_message(void) { return g_last_error.c_str(); }
+const char *fla_last_error(void) { return g_last_error.c_str(); }
 
 fla_status fla_device_error(uint32_t *code) {
   if (!code) return fail(FLA_ERR_INVALID_ARG, "code is NULL");
@@ -113,35 +113,41 @@ fla_status fla_device_error(uint32_t *code) {
 }
 
 // ---------------------------------------------------------------------------
-fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, int64_t ldl,
-                          int64_t n_tokens, int32_t d_model, int32_t n_cols, int32_t dtype,
+fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_cat, void *L, int64_t ldl,
+                          int64_t n_tokens, int32_t d_model, int32_t n_agents, int32_t rank, int32_t dtype,
                           int32_t kernel, fla_stream_t stream) {
   g_last_error.clear();
-  if (n_tokens < 0 || d_model < 1 || n_cols < 1)
-    return fail(FLA_ERR_INVALID_ARG, "n_tokens must be >= 0, d_model and n_cols >= 1");
+  if (n_tokens < 0 || d_model < 1 || n_agents < 1 || rank < 1)
+    return fail(FLA_ERR_INVALID_ARG, "n_tokens must be >= 0; d_model, n_agents and rank >= 1");
+  const int64_t n_cols64 = (int64_t)n_agents * rank;
+  if (n_cols64 > INT32_MAX) return fail(FLA_ERR_INVALID_ARG, "n_agents * rank overflows int32");
+  const int32_t n_cols = (int32_t)n_cols64;
   if (dtype != FLA_F32 && dtype != FLA_BF16) return fail(FLA_ERR_INVALID_ARG, "bad dtype %d", dtype);
   if (kernel < FLA_KERNEL_AUTO || kernel > FLA_KERNEL_TCGEN05)
     return fail(FLA_ERR_INVALID_ARG, "kernel %d is not a fla_kernel", kernel);
   if (ldx < d_model) return fail(FLA_ERR_INVALID_ARG, "ldx (%lld) < d_model (%d)", (long long)ldx, d_model);
-  if (ldl < n_cols) return fail(FLA_ERR_INVALID_ARG, "ldl (%lld) < n_cols (%d)", (long long)ldl, n_cols);
+  if (ldl < n_cols)
+    return fail(FLA_ERR_INVALID_ARG, "ldl (%lld) < n_agents * rank (%d)", (long long)ldl, n_cols);
   if (n_tokens == 0) return ok();
-  if (!X || !A_t || !L) return fail(FLA_ERR_INVALID_ARG, "X, A_t and L must be non-NULL");
+  if (!X || !A_cat || !L) return fail(FLA_ERR_INVALID_ARG, "X, A_cat and L must be non-NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
   if (kernel == FLA_KERNEL_MMA_SYNC)
     return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build has no mma.sync kernel (use TENSOR or TCGEN05)");
-  const bool tc_ok = fla::build_tc_supported(X, ldx, A_t, L, ldl, d_model, n_cols, dtype);
+  const bool tc_ok = fla::build_tc_supported(X, ldx, A_cat, L, ldl, d_model, n_cols, dtype);
   if ((kernel == FLA_KERNEL_TENSOR || kernel == FLA_KERNEL_TCGEN05) && !tc_ok)
     return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build: shape/alignment outside the tensor-core kernel "
-                "(needs bf16, d_model %% 64 == 0, n_cols %% 32 == 0, n_cols <= 512, 16-byte alignment)");
+                "(needs bf16, d_model %% 64 == 0, n_agents * rank %% 32 == 0, 16-byte alignment, "
+                "ldx and ldl multiples of 8)");
   if (tc_ok && kernel != FLA_KERNEL_SIMT) {
-    fla_status st = fla::build_tc_launch(X, ldx, A_t, L, ldl, n_tokens, d_model, n_cols, s);
+    fla_status st = fla::build_tc_launch(X, ldx, A_cat, L, ldl, n_tokens, d_model, n_cols, s);
     if (st != FLA_OK) return fail(st, "lr_cache_build (tensor): %s", fla::build_tc_last_error());
     return check_launch("lr_cache_build (tensor)");
   }
-  fla::SimtBuildParams p{X, A_t, L, ldx, ldl, n_tokens, d_model, n_cols};
+  fla::SimtBuildParams p{X, A_cat, L, ldx, ldl, n_tokens, d_model, n_cols};
   dim3 grid((unsigned)((n_tokens + 63) / 64), (unsigned)((n_cols + 63) / 64));
-  if (grid.x > 0x7fffffffu) return fail(FLA_ERR_UNSUPPORTED, "n_tokens too large");
+  if ((n_tokens + 63) / 64 > 0x7fffffffLL || (n_cols + 63) / 64 > 65535)
+    return fail(FLA_ERR_UNSUPPORTED, "n_tokens or n_agents * rank too large");
   if (dtype == FLA_F32)
     fla::simt_build_kernel<float><<<grid, 256, 0, s>>>(p);
   else
@@ -314,22 +320,46 @@ namespace {
 constexpr int kNoAllocMaxDevices = 64;
 std::mutex g_noalloc_mu;
 void *g_noalloc_ptr[kNoAllocMaxDevices] = {};
+void *g_noalloc_ctx[kNoAllocMaxDevices] = {};  // context the cached address belongs to
+
+typedef CUresult (*PFN_ctxGetCurrent)(CUcontext *);
+
+// The current driver context (nullptr if it cannot be asked).  A device reset
+// destroys the primary context and the next one maps the library image again,
+// possibly elsewhere, so the cached address is only valid for its context.
+void *current_context() {
+  static PFN_ctxGetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_ctxGetCurrent>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 // Device address of the scratch array on the current device.  In host code
 // the array's name only stands in for the symbol, so the address is asked of
-// the runtime once per device, with that device current, and cached.
+// the runtime once per device (and again after a device reset), with that
+// device current, and cached.
 fla_status noalloc_scratch(void **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(FLA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= kNoAllocMaxDevices) return fail(FLA_ERR_UNSUPPORTED, "device index %d out of range", dev);
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+  void *ctx = current_context();
+  if (!g_noalloc_ptr[dev] || ctx != g_noalloc_ctx[dev] || !ctx) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, fla_noalloc_scratch);
     if (e != cudaSuccess || !p)
       return fail(FLA_ERR_CUDA, "cudaGetSymbolAddress(scratch) on device %d: %s", dev, cudaGetErrorString(e));
     g_noalloc_ptr[dev] = p;
+    g_noalloc_ctx[dev] = current_context();  // the lookup may have created the primary context
   }
   *out = g_noalloc_ptr[dev];
   return FLA_OK;

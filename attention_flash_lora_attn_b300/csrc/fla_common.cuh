@@ -22,6 +22,7 @@ enum DeviceErrorCode : uint32_t {
   kErrBuildFullWait = 0x201,    // LR build MMA warp: operands never landed
   kErrBuildEmptyWait = 0x202,   // LR build producer: stage never released
   kErrBuildAccWait = 0x203,     // LR build epilogue: accumulator never committed
+  kErrBuildClusterWait = 0x204, // LR build split-K: a peer CTA never published its partial / finished reading
   kErrPrefillWait = 0x301,      // prefill: any pipeline wait
 };
 

@@ -153,12 +153,12 @@ simt_attn_kernel(const SimtAttnParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// LR-cache build on CUDA cores: L[t, c] = sum_k X[t, k] * A_t[c, k].
+// LR-cache build on CUDA cores: L[t, c] = sum_k X[t, k] * A_cat[k, c].
 // 64x64 output tile per CTA, 256 threads with a 4x4 register tile each,
 // k-steps of 16 staged in shared memory.  fp32 accumulation.
 // ---------------------------------------------------------------------------
 struct SimtBuildParams {
-  const void *X, *At;
+  const void *X, *A;  // A: A_cat [D, N] row-major
   void *L;
   int64_t ldx, ldl, n;
   int32_t D, N;
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(256) simt_build_kernel(const SimtBuildParams p
   __shared__ float xs[16][64 + 1];
   __shared__ float as[16][64 + 1];
   const T *X = reinterpret_cast<const T *>(p.X);
-  const T *At = reinterpret_cast<const T *>(p.At);
+  const T *Ac = reinterpret_cast<const T *>(p.A);
   T *L = reinterpret_cast<T *>(p.L);
   const int64_t row0 = (int64_t)blockIdx.x * 64;
   const int col0 = blockIdx.y * 64;
@@ -181,8 +181,10 @@ __global__ void __launch_bounds__(256) simt_build_kernel(const SimtBuildParams p
       const int64_t gr = row0 + rr;
       const int gk = k0 + kk;
       xs[kk][rr] = (gr < p.n && gk < p.D) ? to_f32(X[gr * p.ldx + gk]) : 0.f;
-      const int gc = col0 + rr;
-      as[kk][rr] = (gc < p.N && gk < p.D) ? to_f32(At[(int64_t)gc * p.D + gk]) : 0.f;
+      // A_cat rows are contiguous along the columns: consecutive threads read consecutive columns
+      const int ak = e / 64, ac = e % 64;
+      const int gc = col0 + ac, gka = k0 + ak;
+      as[ak][ac] = (gc < p.N && gka < p.D) ? to_f32(Ac[(int64_t)gka * p.N + gc]) : 0.f;
     }
     __syncthreads();
 #pragma unroll

@@ -173,6 +173,8 @@ def barrier(world_size: int):
 
 
 PREROLL_S = 0.25
+REPLAYS = 21      # timed replays of the headline's K-step graph (median reported)
+E2E_ROUNDS = 5    # timed rounds of the host-buffer loop (median reported)
 
 
 def preroll(fn, stream, seconds=PREROLL_S):
@@ -285,19 +287,26 @@ def run_ours(args, ws, rank, local):
     calls = [make_call(c) for c in copies]
     graph = time_graph(calls, args.steps, args.warmup, stream)
 
-    # ---- timed region: K steps from the graph, events on the launching stream
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # ---- timed regions: REPLAYS replays of the K-step graph, each bracketed by
+    #      a barrier + synchronize and timed with CUDA events on the launching
+    #      stream; the line reports the median (and the min-max spread)
+    times = []
     barrier(ws)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk, torch.cuda.stream(stream):
         preroll(graph.replay, stream)
-        # replay() launches on the current stream, which is `stream` here
-        start.record(stream)
-        graph.replay()
-        end.record(stream)
-        torch.cuda.synchronize()
+        for _ in range(REPLAYS):
+            start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            barrier(ws)
+            torch.cuda.synchronize()
+            # replay() launches on the current stream, which is `stream` here
+            start.record(stream)
+            graph.replay()
+            end.record(stream)
+            torch.cuda.synchronize()
+            times.append(start.elapsed_time(end) / 1e3)
     barrier(ws)
-    t_local = start.elapsed_time(end) / 1e3
+    t_local = statistics.median(times)
     t = max_over_ranks(t_local, ws, device)
     queries_per_step = w.n_req * w.n_agents
     value = ws * queries_per_step * args.steps / t
@@ -322,17 +331,22 @@ def run_ours(args, ws, rank, local):
         for c in calls:
             c()
 
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_times = []
     barrier(ws)
     torch.cuda.synchronize()
     preroll(e2e_round, stream)
-    e0.record(stream)
-    for i in range(args.steps):
-        calls[i % n_copies]()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    for _ in range(E2E_ROUNDS):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(ws)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            calls[i % n_copies]()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_times.append(e0.elapsed_time(e1) / 1e3)
     barrier(ws)
-    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, ws, device)
+    t_e2e = max_over_ranks(statistics.median(e2e_times), ws, device)
     e2e_value = ws * queries_per_step * args.steps / t_e2e
 
     peaks = load_peaks()
@@ -358,9 +372,12 @@ def run_ours(args, ws, rank, local):
             "context_tokens": w.total_tokens, "queries_per_step": queries_per_step,
             "parallelism": f"replicas x{ws} (independent workloads, no collective)",
             "l2": f"inputs rotate over {n_copies} copies ({n_copies * per_copy / 1e6:.0f} MB > 4x the 126 MB L2)",
-            "timing": "CUDA graph of K decode launches, CUDA events on the launching stream; the timed "
-                      f"replay follows {PREROLL_S:.2f} s of untimed replays of the same graph (load clocks; "
-                      "the clock samples fall in that window)",
+            "timing": f"median of {REPLAYS} replays of a CUDA graph of K back-to-back decode calls, each "
+                      "replay bracketed by a barrier + synchronize and timed with CUDA events on the launching "
+                      f"stream, after {PREROLL_S:.2f} s of untimed replays of the same graph (load clocks)",
+            "replays": REPLAYS,
+            "ms_per_step_min": min(times) / args.steps * 1e3,
+            "ms_per_step_max": max(times) / args.steps * 1e3,
         },
         "roofline": {
             "bound": "hbm",
@@ -377,7 +394,10 @@ def run_ours(args, ws, rank, local):
         "e2e": {"value": e2e_value, "unit": "queries/s",
                 "h2d_bytes_per_step": int(copies[0]["Q"].numel() * 2),
                 "d2h_bytes_per_step": int(copies[0]["O"].numel() * 4),
-                "api": "flash_lora_attn_decode_host_io (pinned host Q in, host O out, one call per step)"},
+                "api": "flash_lora_attn_decode_host_io (pinned host Q in, host O out, one call per step)",
+                "timing": f"median of {E2E_ROUNDS} rounds of K steps",
+                "ms_per_step_min": min(e2e_times) / args.steps * 1e3,
+                "ms_per_step_max": max(e2e_times) / args.steps * 1e3},
         # per step: the decode kernel and the split-merge kernel behind it
         "gpu_launches": 2 * args.steps,
         "clocks": clk.summary(),
@@ -386,6 +406,15 @@ def run_ours(args, ws, rank, local):
     torch.cuda.empty_cache()
     if rank == 0 and args.legs == "all":
         line["legs"] = run_legs(args, device, peaks)
+        iso = line["legs"].get(f"{HEADLINE}/decode")
+        if iso:
+            line["latency"] = {
+                "isolated_call_us": iso["us"],
+                "isolated_call_hbm_frac": iso["hbm_frac"],
+                "pipelined_call_us": ms_per_step * 1e3,
+                "pipelined_call_hbm_frac": achieved_gbs / peaks["hbm_gbs"],
+                "note": "isolated: one call alone, L2 flushed before it, median of event-timed graph "
+                        "replays; pipelined: the headline's back-to-back calls"}
     if rank == 0 and ws == 1:
         line["cpu_baseline"] = cpu_baseline(w)
     return line
@@ -455,10 +484,10 @@ def run_legs(args, device, peaks, only=None):
     # ---- LR-cache build of a 512-token chunk (4 agents, r 16) and the causal chunked prefill
     w = WORKLOADS["llama8b_prefill"]
     A, r, D, c, n0 = w.n_agents, w.rank, w.d_model, w.chunk, w.n0
-    X, A_t = rnd((c, D)), rnd((A * r, D), D ** -0.5)
+    X, A_cat = rnd((c, D)), rnd((D, A * r), D ** -0.5)
     L = rnd((n0 + c, A * r))
     if want("llama8b_prefill/lr_cache_build"):
-        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_t, L[n0:]), reps, stream, flush)
+        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_cat, L[n0:], n_agents=A), reps, stream, flush)
         flops, byts = 2 * c * D * A * r, (c * D + A * r * D + c * A * r) * 2
         out["llama8b_prefill/lr_cache_build"] = {
             "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
@@ -475,7 +504,7 @@ def run_legs(args, device, peaks, only=None):
         out["llama8b_prefill/prefill"] = {"us": t * 1e6, "tflops": flops / t / 1e12,
                                           "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"]}
         del Q, K, V, B, O
-    del X, A_t, L
+    del X, A_cat, L
     # ---- decode legs (inputs larger than L2)
     for name in ("llama8b_decode", "llama8b_ragged", "llama70b_decode"):
         if not want(f"{name}/decode"):
@@ -547,14 +576,14 @@ def run_legs(args, device, peaks, only=None):
         if not want(leg) or (only is None and rows != w.build_tokens):
             continue
         n, D, Nc = rows, w.d_model, w.n_agents * w.rank
-        X, A_t = rnd((n, D)), rnd((Nc, D), D ** -0.5)
+        X, A_cat = rnd((n, D)), rnd((D, Nc), D ** -0.5)
         L = torch.empty((n, Nc), dtype=torch.bfloat16, device=device)
-        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_t, L), max(3, reps // 2), stream)
+        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_cat, L, n_agents=w.n_agents), max(3, reps // 2), stream)
         flops, byts = 2 * n * D * Nc, (n * D + Nc * D + n * Nc) * 2
         out[leg] = {
             "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
             "gbs": byts / t / 1e9, "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
-        del X, A_t, L
+        del X, A_cat, L
     del scratch
     torch.cuda.empty_cache()
     assert fla.device_error() == 0
@@ -586,11 +615,116 @@ def oracle_sample_rate(w, budget_s=10.0, max_reps=50):
     return reps / t_total, reps, t_total, cores, threads
 
 
+def _rate(fn, budget_s, max_reps, min_reps=1):
+    """(reps / seconds, reps, seconds) of fn() repeated until budget_s or max_reps."""
+    reps, t_total = 0, 0.0
+    while reps < min_reps or (reps < max_reps and t_total < budget_s):
+        t0 = time.perf_counter()
+        fn(reps)
+        t_total += time.perf_counter() - t0
+        reps += 1
+    return reps / t_total, reps, t_total
+
+
+def oracle_per_config():
+    """The oracle timed on every workload (bounded samples, extrapolated where
+    the full workload would take minutes); all host threads unless stated."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+    from threadpoolctl import threadpool_limits
+
+    import oracle
+    from workloads import WORKLOADS, make_build_inputs, make_decode_inputs, make_prefill_inputs
+
+    out = {}
+
+    def decode_one(x, q, a, r):
+        o = x["offsets"]
+        t0, t1 = int(o[q]), int(o[q + 1])
+        oracle.decode(x["Q"][q:q + 1, a:a + 1], x["K_base"][t0:t1], x["V_base"][t0:t1],
+                      x["L"][t0:t1, a * r:(a + 1) * r], x["B"][a:a + 1], np.array([0, t1 - t0]), rank=r)
+
+    # c0: the whole tiny fp32 workload (2 queries) per repetition
+    w = WORKLOADS["tiny_decode"]
+    x = make_decode_inputs(w, seed=0)
+    for tag, limit in (("", None), ("_1thread", 1)):
+        with threadpool_limits(limits=limit):
+            rate, reps, secs = _rate(lambda i: oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"],
+                                                             x["offsets"].numpy(), rank=w.rank), 1.0, 200)
+        out["tiny_decode" + tag] = {"value": rate * w.n_req * w.n_agents, "unit": "queries/s",
+                                    "sample": f"{reps} runs of the full workload, {secs:.2f} s"}
+    # c1: single-agent queries of the headline decode
+    w = WORKLOADS["llama8b_decode"]
+    x = make_decode_inputs(w, seed=0)
+    for tag, limit, budget in (("", None, 4.0), ("_1thread", 1, 4.0)):
+        with threadpool_limits(limits=limit):
+            rate, reps, secs = _rate(lambda i: decode_one(x, 0, i % w.n_agents, w.rank), budget, 50)
+        out["llama8b_decode" + tag] = {"value": rate, "unit": "queries/s",
+                                       "sample": f"{reps} single-agent queries (all heads, 16384 tokens), "
+                                                 f"{secs:.2f} s"}
+    del x
+    # c2: causal prefill positions (one agent, all heads) and the chunk's LR build
+    w = WORKLOADS["llama8b_prefill"]
+    x = make_prefill_inputs(w, seed=0)
+    r = w.rank
+    pos = [0, 255, 511]
+
+    def prefill_one(i):
+        a, p = i % w.n_agents, pos[i % len(pos)]
+        oracle.prefill(x["Q"][a:a + 1], x["K_base"], x["V_base"], x["L"][:, a * r:(a + 1) * r], x["B"][a:a + 1],
+                       n0=w.n0, rank=r, positions=[p])
+    rate, reps, secs = _rate(prefill_one, 3.0, 30)
+    out["llama8b_prefill/prefill"] = {
+        "value": rate, "unit": "query tokens/s",
+        "sample": f"{reps} (agent, chunk position) rows, all heads, {secs:.2f} s",
+        "full_chunk_s_extrapolated": w.n_agents * w.chunk / rate}
+    rate, reps, secs = _rate(lambda i: oracle.lr_cache_build(x["X"], x["A_cat"]), 2.0, 20)
+    out["llama8b_prefill/lr_cache_build"] = {
+        "value": rate * w.chunk, "unit": "rows/s",
+        "gflops": rate * 2 * w.chunk * w.d_model * w.n_agents * r / 1e9,
+        "sample": f"{reps} full 512x4096 . 4096x64 builds, {secs:.2f} s"}
+    del x
+    # c3: single-agent queries of the shortest, a middle and the longest request;
+    #     the batch time is extrapolated by tokens (each query's cost grows with
+    #     its request's length)
+    w = WORKLOADS["llama8b_ragged"]
+    lens = sorted(w.lengths)
+    pick = [lens[0], lens[len(lens) // 2], lens[-1]]
+    x = make_decode_inputs(dataclasses.replace(w, lengths=tuple(pick)), seed=0)
+    rate, reps, secs = _rate(lambda i: decode_one(x, i % 3, i % w.n_agents, w.rank), 3.0, 30, min_reps=3)
+    toks = sum(pick[i % 3] for i in range(reps))
+    batch_s = secs / toks * w.total_tokens * w.n_agents
+    out["llama8b_ragged"] = {"value": w.n_req * w.n_agents / batch_s, "unit": "queries/s",
+                             "sample": f"{reps} single-agent queries on requests of {pick} tokens, {secs:.2f} s; "
+                                       "batch time extrapolated by tokens",
+                             "batch_s_extrapolated": batch_s}
+    del x
+    # c4: one agent's query over the full 131072-token context, and 512 sampled
+    #     rows of the 131072 x 8192 . 8192 x 320 build (extrapolated to all rows)
+    w = WORKLOADS["llama70b_decode"]
+    x = make_decode_inputs(w, seed=0)
+    rate, reps, secs = _rate(lambda i: decode_one(x, 0, i % w.n_agents, w.rank), 1.0, 2)
+    out["llama70b_decode"] = {"value": rate, "unit": "queries/s",
+                              "sample": f"{reps} single-agent queries (all 64 heads, 131072 tokens), {secs:.2f} s"}
+    del x
+    b = make_build_inputs(512, w.d_model, w.n_agents, w.rank, torch.bfloat16, seed=0)
+    rate, reps, secs = _rate(lambda i: oracle.lr_cache_build(b["X"], b["A_cat"]), 2.0, 20)
+    out["llama70b_decode/lr_cache_build"] = {
+        "value": rate * 512, "unit": "rows/s",
+        "gflops": rate * 2 * 512 * w.d_model * w.n_agents * w.rank / 1e9,
+        "sample": f"{reps} builds of 512 sampled rows, {secs:.2f} s",
+        "full_build_s_extrapolated": w.build_tokens / (rate * 512)}
+    return out
+
+
 def cpu_baseline(w):
     rate, reps, secs, cores, threads = oracle_sample_rate(w)
     return {"value": rate, "unit": "queries/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} single-agent decode queries (all 32 heads, 16384 tokens) of the "
-                      f"headline workload, fp64 numpy, {secs:.1f} s; BLAS threads {threads}"}
+                      f"headline workload, fp64 numpy, {secs:.1f} s; BLAS threads {threads}",
+            "per_config": oracle_per_config()}
 
 
 def run_reference(args):

@@ -23,7 +23,7 @@
  *     asynchronous and never synchronise the host.
  *   - Arguments are validated on the host before anything is launched; an
  *     invalid call returns an error status and launches nothing.
- *   - Errors never cross the ABI as exceptions.  fla_last_error_message()
+ *   - Errors never cross the ABI as exceptions.  fla_last_error()
  *     returns a thread-local description of the last failure.
  *   - Device-side waits are bounded.  A kernel whose wait runs out sets a
  *     device error word and returns early (its outputs are then undefined);
@@ -94,28 +94,32 @@ typedef struct {
 } fla_attn_dims;
 
 /*
- * lr_cache_build - L[t, c] = sum_k X[t, k] * A_t[c, k]   (L = X . A_cat)
+ * lr_cache_build - L = X . A_cat, i.e. L[t, c] = sum_k X[t, k] * A_cat[k, c]
  *
  * LRAgent summary, Metodologia section 2 (BaseShared: the LR cache stores the
  * LoRA down-projection X.A_i at width r); PReCache abstract (PreLRShared:
  * all agents' LR caches built in one pass over the context).
  *
- *   X      [n_tokens, d_model], row stride ldx elements      (input)
- *   A_t    [n_cols, d_model], dense: row c is column c of A_cat = [A_1|...|A_A],
- *          i.e. the stacked nn.Linear weights of the agents' down-projections,
- *          agent-major (agent i owns rows [i*r, (i+1)*r))    (input)
- *   L      [n_tokens, n_cols] written with row stride ldl elements (output;
- *          other columns of a wider L are left untouched)
- *   dtype  storage type of X, A_t and L; fp32 accumulation.
- *   kernel fla_kernel.  The tensor-core path needs bf16, d_model % 64 == 0,
- *          n_cols % 32 == 0, n_cols <= 512, 16-byte aligned pointers and
- *          ldx, ldl multiples of 8.
+ *   X        [n_tokens, d_model], row stride ldx elements    (input)
+ *   A_cat    [d_model, n_agents * rank], dense row-major: the agents'
+ *            down-projections side by side, A_cat = [A_1 | ... | A_A], agent i
+ *            owning columns [i*rank, (i+1)*rank)               (input)
+ *   L        [n_tokens, n_agents * rank] written with row stride ldl elements
+ *            (output; column block i is agent i's LR cache L_i = X . A_i;
+ *            other columns of a wider L are left untouched)
+ *   dtype    storage type of X, A_cat and L; fp32 accumulation.
+ *   kernel   fla_kernel.  The tensor-core (tcgen05) path needs bf16,
+ *            d_model % 64 == 0, n_agents * rank % 32 == 0, 16-byte aligned
+ *            pointers and ldx, ldl multiples of 8; wider products are tiled
+ *            over 512-column tiles, and short inputs split d_model over a
+ *            thread-block cluster.  SIMT covers every other shape.
  * Errors: FLA_ERR_INVALID_ARG for null pointers with n_tokens > 0, negative
- * sizes, ldx < d_model or ldl < n_cols.  n_tokens == 0 is a no-op.
+ * sizes, n_agents or rank < 1, ldx < d_model or ldl < n_agents * rank.
+ * n_tokens == 0 is a no-op.
  */
-FLA_API fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_t, void *L, int64_t ldl,
-                          int64_t n_tokens, int32_t d_model, int32_t n_cols, int32_t dtype,
-                          int32_t kernel, fla_stream_t stream);
+FLA_API fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_cat, void *L, int64_t ldl,
+                                  int64_t n_tokens, int32_t d_model, int32_t n_agents, int32_t rank,
+                                  int32_t dtype, int32_t kernel, fla_stream_t stream);
 
 /*
  * flash_lora_attn_decode - one query token per agent per request.
@@ -207,7 +211,9 @@ FLA_API fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     that first call before any stream capture.  The cache is keyed on the
+ *     device's current context, so after cudaDeviceReset the next call looks
+ *     the address up again (make that call outside a capture too).
  *   - Every call on a device shares the one array; it needs no zeroing (each
  *     call writes every scratch value before reading it) and keeps the last
  *     call's contents.  Calls on one device that may overlap on the GPU (for
@@ -282,7 +288,7 @@ FLA_API fla_status flash_lora_attn_decode_host_io(const fla_attn_dims *dims, con
 FLA_API const char *fla_status_string(fla_status status);
 
 /* Description of the last failure on the calling thread ("" if none). */
-FLA_API const char *fla_last_error_message(void);
+FLA_API const char *fla_last_error(void);
 
 /* Reads, and resets to 0, the device error word of the current device.
  * Synchronises the device first.  Writes 0 (no error) or a nonzero code that

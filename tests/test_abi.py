@@ -58,7 +58,7 @@ def _decode(lib, dims, n_req=1, total=16, ptr=16, ws=None, ws_bytes=0):
 
 def test_decode_rejects_bad_shapes_without_launching(lib):
     assert _decode(lib, _dims(hq=30)) == 1            # hq % hkv
-    assert "multiple of hkv" in lib.fla_last_error_message().decode()
+    assert "multiple of hkv" in lib.fla_last_error().decode()
     assert _decode(lib, _dims(n_agents=0)) == 1
     assert _decode(lib, _dims(head_dim=130)) == 2     # not a multiple of 4
     assert _decode(lib, _dims(rank=0)) == 2
@@ -98,14 +98,14 @@ def test_kernel_generation_selection_is_validated(lib):
     h = _dims(head_dim=64)
     h.kernel = 4                                       # the tcgen05 decode kernel needs head_dim 128
     assert _decode(lib, h) == 2
-    assert "tcgen05" in lib.fla_last_error_message().decode()
-    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 1, 3, None) == 2   # build has no mma.sync kernel
-    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 0, 4, None) == 2   # fp32: outside tcgen05
+    assert "tcgen05" in lib.fla_last_error().decode()
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 1, 16, 1, 3, None) == 2   # build has no mma.sync kernel
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 1, 16, 0, 4, None) == 2   # fp32: outside tcgen05
     # prefill: L width A*r = 96 > 64 is outside the tcgen05 kernel; refused before any launch
     w = _dims(n_agents=3, rank=32, l_row_stride=96, l_agent_stride=32)
     w.kernel = 4
     assert lib.flash_lora_attn_prefill(ctypes.byref(w), p, p, p, p, p, 1, 20, p, None, 0, None) == 2
-    assert "tcgen05" in lib.fla_last_error_message().decode()
+    assert "tcgen05" in lib.fla_last_error().decode()
     f = _dims(dtype_code=0)
     f.kernel = 3
     assert lib.flash_lora_attn_prefill(ctypes.byref(f), p, p, p, p, p, 1, 20, p, None, 0, None) == 2
@@ -116,21 +116,24 @@ def test_empty_calls_are_noops(lib):
     d = _dims()
     p = ctypes.c_void_p(16)
     assert lib.flash_lora_attn_prefill(ctypes.byref(d), p, p, p, p, p, 0, 0, p, None, 0, None) == 0
-    assert lib.lr_cache_build(p, 64, p, p, 16, 0, 64, 16, 1, 0, None) == 0
+    assert lib.lr_cache_build(p, 64, p, p, 16, 0, 64, 1, 16, 1, 0, None) == 0
 
 
 def test_build_rejects_bad_arguments(lib):
     p = ctypes.c_void_p(16)
-    assert lib.lr_cache_build(p, 32, p, p, 16, 8, 64, 16, 1, 0, None) == 1   # ldx < d_model
-    assert lib.lr_cache_build(p, 64, p, p, 8, 8, 64, 16, 1, 0, None) == 1    # ldl < n_cols
-    assert lib.lr_cache_build(None, 64, p, p, 16, 8, 64, 16, 1, 0, None) == 1
-    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 5, 0, None) == 1   # dtype
+    assert lib.lr_cache_build(p, 32, p, p, 16, 8, 64, 1, 16, 1, 0, None) == 1   # ldx < d_model
+    assert lib.lr_cache_build(p, 64, p, p, 8, 8, 64, 1, 16, 1, 0, None) == 1    # ldl < n_cols
+    assert lib.lr_cache_build(None, 64, p, p, 16, 8, 64, 1, 16, 1, 0, None) == 1
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 1, 16, 5, 0, None) == 1   # dtype
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 0, 16, 1, 0, None) == 1   # n_agents < 1
+    assert lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 1, 0, 1, 0, None) == 1    # rank < 1
+    assert lib.lr_cache_build(p, 64, p, p, 32, 8, 64, 4, 16, 1, 0, None) == 1   # ldl < n_agents * rank
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     p = ctypes.c_void_p(16)
-    st = lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 16, 1, 1, None)
+    st = lib.lr_cache_build(p, 64, p, p, 16, 8, 64, 1, 16, 1, 1, None)
     assert st == 4
 
 

@@ -303,9 +303,8 @@ def test_prefill_llama8b_chunk_with_lr_build_sampled_rows(kernel):
     w = WORKLOADS["llama8b_prefill"]
     x = make_prefill_inputs(w, seed=0)
     dx = to_dev(x)
-    A_t = dx["A_cat"].t().contiguous()
     fla = _fla()
-    fla.lr_cache_build(dx["X"], A_t, dx["L"][w.n0:])
+    fla.lr_cache_build(dx["X"], dx["A_cat"], dx["L"][w.n0:], n_agents=w.n_agents)
     O = fla.flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], w.n0,
                                     rank=w.rank, kernel=kernel).cpu()
     # oracle: its own LR rows for the chunk (fp64 product rounded to the bf16 storage type)
@@ -332,7 +331,7 @@ def test_lr_build_small(case, kernel):
     n, D, N, dt = case
     dtype = torch.bfloat16 if dt == "bf16" else torch.float32
     x = make_build_inputs(n, D, 1, N, dtype, seed=4)
-    dX, dA = x["X"].cuda(), x["A_cat"].t().contiguous().cuda()
+    dX, dA = x["X"].cuda(), x["A_cat"].cuda()
     L = _fla().lr_cache_build(dX, dA, kernel=kernel).double().cpu().numpy()
     ref = oracle.lr_cache_build(x["X"], x["A_cat"])
     assert _rel_l2(L, ref) <= (BUILD_RTOL_L2 if dt == "bf16" else 1e-6)
@@ -344,7 +343,7 @@ def test_lr_build_tensor_kernel(case):
     """The tcgen05 GEMM itself (kernel="tensor" refuses to fall back)."""
     n, D, N = case
     x = make_build_inputs(n, D, 1, N, torch.bfloat16, seed=8)
-    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].t().contiguous().cuda(), kernel="tensor")
+    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].cuda(), kernel="tensor")
     ref = oracle.lr_cache_build(x["X"], x["A_cat"])
     assert _rel_l2(L.double().cpu().numpy(), ref) <= BUILD_RTOL_L2
 
@@ -352,7 +351,7 @@ def test_lr_build_tensor_kernel(case):
 def test_lr_build_strided_output_leaves_other_columns():
     x = make_build_inputs(200, 512, 2, 32, torch.bfloat16, seed=6)
     L = torch.full((200, 100), 7.0, dtype=torch.bfloat16, device="cuda")
-    _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].t().contiguous().cuda(), L[:, 8:72])
+    _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].cuda(), L[:, 8:72])
     Lc = L.double().cpu().numpy()
     assert (Lc[:, :8] == 7).all() and (Lc[:, 72:] == 7).all()
     assert _rel_l2(Lc[:, 8:72], oracle.lr_cache_build(x["X"], x["A_cat"])) <= BUILD_RTOL_L2
@@ -360,7 +359,7 @@ def test_lr_build_strided_output_leaves_other_columns():
 
 def test_lr_build_llama8b_chunk_full():
     x = make_build_inputs(512, 4096, 4, 16, torch.bfloat16, seed=0)
-    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].t().contiguous().cuda(), kernel="tensor")
+    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].cuda(), kernel="tensor")
     assert _rel_l2(L.double().cpu().numpy(), oracle.lr_cache_build(x["X"], x["A_cat"])) <= BUILD_RTOL_L2
 
 
@@ -368,7 +367,7 @@ def test_lr_build_llama70b_full_size_sampled_rows():
     """131072 x 8192 . 8192 x 320 on the GPU; 4096 sampled rows against the oracle."""
     x = make_build_inputs(131072, 8192, 5, 64, torch.bfloat16, seed=0)
     dX = x["X"].cuda()
-    L = _fla().lr_cache_build(dX, x["A_cat"].t().contiguous().cuda(), kernel="tensor")
+    L = _fla().lr_cache_build(dX, x["A_cat"].cuda(), kernel="tensor")
     rows = np.sort(np.random.default_rng(0).choice(131072, 4096, replace=False))
     rows = np.concatenate([[0, 1], rows, [131070, 131071]])
     Ls = L[torch.from_numpy(rows).cuda()].double().cpu().numpy()

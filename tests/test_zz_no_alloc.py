@@ -5,9 +5,11 @@ serving loop whose memory budget is fixed at start-up, a plugin whose host
 framework owns every allocation).  This entry point takes no workspace; the
 split-context partials live in a fixed 16 MiB array inside the library.  The
 test calls it through the C ABI twice in a row and compares each result with
-the regular entry point's (which gets a caller-provided workspace), within
-the tolerance the parity tests use.  It must pass alone in a fresh process
-and after the other tests, so it builds and loads the library itself.
+the regular entry point's (which gets a caller-provided workspace) and with
+the fp64 oracle, within the tolerance the parity tests use, on both decode
+kernels (12 query rows per kv head: mma.sync; 40: tcgen05, whose partial
+records are laid out differently).  It must pass alone in a fresh process and
+after the other tests, so it builds and loads the library itself.
 """
 import ctypes
 
@@ -15,6 +17,9 @@ import numpy as np
 import pytest
 import torch
 
+import dataclasses
+
+import oracle
 from workloads import WORKLOADS, make_decode_inputs
 
 pytestmark = pytest.mark.gpu
@@ -51,23 +56,34 @@ def _noalloc(fla, x, rank, O):
         ctypes.byref(dims), x["Q"].data_ptr(), x["K_base"].data_ptr(), x["V_base"].data_ptr(), x["L"].data_ptr(),
         x["B"].data_ptr(), x["offsets"].data_ptr(), R, N, O.data_ptr(),
         torch.cuda.current_stream().cuda_stream)
-    assert st == 0, lib.fla_last_error_message()
+    assert st == 0, lib.fla_last_error()
     return O
 
 
-@pytest.mark.parametrize("name,lengths", [("llama8b_decode", None), ("llama8b_decode", [3000, 17, 1, 9000])],
-                         ids=["single-request", "ragged"])
-def test_noalloc_matches_workspace_decode_twice(fla, name, lengths):
-    w = WORKLOADS[name]
-    x = {k: v.cuda() for k, v in make_decode_inputs(w, seed=21, lengths=lengths).items()}
+CASES = {
+    "mma-single-request": (WORKLOADS["llama8b_decode"], None),
+    "mma-ragged": (WORKLOADS["llama8b_decode"], [3000, 17, 1, 9000]),
+    "tcgen05-70b-group": (dataclasses.replace(WORKLOADS["llama70b_decode"], lengths=(6000,)), None),
+    "tcgen05-ragged": (dataclasses.replace(WORKLOADS["llama70b_decode"], lengths=(1000, 0, 200)), None),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_noalloc_matches_workspace_decode_and_oracle_twice(fla, case):
+    w, lengths = CASES[case]
+    xh = make_decode_inputs(w, seed=21, lengths=lengths)
+    x = {k: v.cuda() for k, v in xh.items()}
     ws = torch.empty(1 << 24, dtype=torch.uint8, device="cuda")
     ref = fla.flash_lora_attn_decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], x["offsets"], rank=w.rank,
                                      workspace=ws)
+    want = oracle.decode(xh["Q"], xh["K_base"], xh["V_base"], xh["L"], xh["B"], xh["offsets"].numpy(),
+                         rank=w.rank)
     for _ in range(2):  # two calls in a row share the fixed scratch array
         O = torch.full_like(ref, float("nan"))
         _noalloc(fla, x, w.rank, O)
         torch.cuda.synchronize()
         _close(O, ref)
+        _close(O, torch.from_numpy(want))
     assert fla.device_error() == 0
 
 
@@ -78,4 +94,4 @@ def test_noalloc_rejects_calls_needing_more_scratch(fla):
     p = ctypes.c_void_p(256)  # never dereferenced: the size check comes first
     st = lib.flash_lora_attn_decode_noalloc(ctypes.byref(dims), p, p, p, p, p, p, 4096, 1 << 30, p, None)
     assert st == 3  # FLA_ERR_WORKSPACE
-    assert b"16777216" in lib.fla_last_error_message()
+    assert b"16777216" in lib.fla_last_error()
