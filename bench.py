@@ -633,12 +633,11 @@ def oracle_per_config():
 
     import numpy as np
     import torch
-    from threadpoolctl import threadpool_limits
-
     import oracle
     from workloads import WORKLOADS, make_build_inputs, make_decode_inputs, make_prefill_inputs
 
     out = {}
+    one_thread = os.environ.get("FLA_ORACLE_ONE_THREAD") == "1"
 
     def decode_one(x, q, a, r):
         o = x["offsets"]
@@ -649,22 +648,19 @@ def oracle_per_config():
     # c0: the whole tiny fp32 workload (2 queries) per repetition
     w = WORKLOADS["tiny_decode"]
     x = make_decode_inputs(w, seed=0)
-    for tag, limit in (("", None), ("_1thread", 1)):
-        with threadpool_limits(limits=limit):
-            rate, reps, secs = _rate(lambda i: oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"],
-                                                             x["offsets"].numpy(), rank=w.rank), 1.0, 200)
-        out["tiny_decode" + tag] = {"value": rate * w.n_req * w.n_agents, "unit": "queries/s",
-                                    "sample": f"{reps} runs of the full workload, {secs:.2f} s"}
+    rate, reps, secs = _rate(lambda i: oracle.decode(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"],
+                                                     x["offsets"].numpy(), rank=w.rank), 1.0, 200)
+    out["tiny_decode"] = {"value": rate * w.n_req * w.n_agents, "unit": "queries/s",
+                          "sample": f"{reps} runs of the full workload, {secs:.2f} s"}
     # c1: single-agent queries of the headline decode
     w = WORKLOADS["llama8b_decode"]
     x = make_decode_inputs(w, seed=0)
-    for tag, limit, budget in (("", None, 4.0), ("_1thread", 1, 4.0)):
-        with threadpool_limits(limits=limit):
-            rate, reps, secs = _rate(lambda i: decode_one(x, 0, i % w.n_agents, w.rank), budget, 50)
-        out["llama8b_decode" + tag] = {"value": rate, "unit": "queries/s",
-                                       "sample": f"{reps} single-agent queries (all heads, 16384 tokens), "
-                                                 f"{secs:.2f} s"}
+    rate, reps, secs = _rate(lambda i: decode_one(x, 0, i % w.n_agents, w.rank), 4.0, 50)
+    out["llama8b_decode"] = {"value": rate, "unit": "queries/s",
+                             "sample": f"{reps} single-agent queries (all heads, 16384 tokens), {secs:.2f} s"}
     del x
+    if one_thread:
+        return out
     # c2: causal prefill positions (one agent, all heads) and the chunk's LR build
     w = WORKLOADS["llama8b_prefill"]
     x = make_prefill_inputs(w, seed=0)
@@ -719,12 +715,27 @@ def oracle_per_config():
     return out
 
 
+def oracle_one_thread():
+    """The c0 and c1 oracle rates with one host thread: a child process whose
+    BLAS and OpenMP pools are limited to one thread before numpy loads."""
+    env = dict(os.environ, FLA_ORACLE_ONE_THREAD="1", OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+               MKL_NUM_THREADS="1")
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-per-config"], env=env,
+                       capture_output=True, text=True, timeout=300)
+    if r.returncode != 0:
+        return {"error": (r.stderr or r.stdout)[-300:]}
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    return {f"{k}_1thread": v for k, v in res.items()}
+
+
 def cpu_baseline(w):
     rate, reps, secs, cores, threads = oracle_sample_rate(w)
+    per = oracle_per_config()
+    per.update(oracle_one_thread())
     return {"value": rate, "unit": "queries/s", "cores": cores, "kind": "oracle",
             "sample": f"{reps} single-agent decode queries (all 32 heads, 16384 tokens) of the "
                       f"headline workload, fp64 numpy, {secs:.1f} s; BLAS threads {threads}",
-            "per_config": oracle_per_config()}
+            "per_config": per}
 
 
 def run_reference(args):
@@ -787,12 +798,21 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--legs", choices=["all", "none"], default="all")
+    ap.add_argument("--oracle-per-config", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--only", default=None,
                     help="run one leg alone (e.g. llama70b_decode/decode) and print its numbers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()
+
+    if args.oracle_per_config:  # child of oracle_one_thread()
+        if os.environ.get("FLA_ORACLE_ONE_THREAD") == "1":
+            import torch
+
+            torch.set_num_threads(1)
+        print(json.dumps(oracle_per_config()))
+        return 0
 
     if args.only:
         import torch
