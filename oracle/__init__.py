@@ -15,6 +15,9 @@ kernel's reordering:
   output, V_i = V_base + L_i . B_i.  The oracle materialises V_i at full
   width, exactly the "naive reconstruction" that section 3
   ("Flash-LoRA-Attention", Problema bullet) describes.
+* Base-cache rebuild (PReCache abstract, ReBaseShared): K_base = X . W_k and
+  V_base = X . W_v from adapter-free hidden states with the pretrained
+  weights, computed together with every agent's L_i = X . A_i.
 * Attention: O = softmax(q . K_base^T / sqrt(d)) . V_i, softmax taken with
   the maximum subtracted, all in fp64.  Keys carry no adapter term.
 
@@ -29,10 +32,12 @@ Pins (tests/test_oracle.py): hand-derived tiny cases in tests/golden/,
 B = 0 against torch's scaled_dot_product_attention in fp64, Q = 0 against
 the mean of V_i, reordered vs materialised, causal visibility, GQA against
 duplicated-head MHA, ragged against separate requests, token permutation,
-n = 1, and lr_cache_build against brute-force sums on integer inputs.
+n = 1, lr_cache_build against brute-force sums on integer inputs, and
+rebase_kv_lr_build against a hand-derived case, brute force and closed forms.
 """
 from .reference import (  # noqa: F401
     lr_cache_build,
+    rebase_kv_lr_build,
     agent_value_cache,
     decode,
     decode_reordered,

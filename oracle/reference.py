@@ -10,9 +10,11 @@ Sources are cited by page and section:
                (BaseShared and BaseLRShared bullets).
   [LRAgent-3]  same page, section 3 "Flash-LoRA-Attention".
   [PReCache]   PReCache abstract (arxivdaily), PreLRShared paragraph.
+  [ReBase]     same abstract, ReBaseShared paragraph (the shared base cache
+               rebuilt from adapter-free hidden states with the pretrained
+               weights).
 
-Readings taken where the pages are silent (each is also listed in the
-design notes):
+Readings taken where the pages are silent:
   * softmax scale is 1/sqrt(d) unless the caller passes another value;
   * the adapter acts on values only; keys are base-only;
   * LoRA's alpha/r factor is folded into B (no extra scale);
@@ -61,6 +63,27 @@ def lr_cache_build(X, A_cat) -> np.ndarray:
     context is first processed".
     """
     return to_f64(X) @ to_f64(A_cat)
+
+
+def rebase_kv_lr_build(X, W_k, W_v, A_cat, hkv: int, d: int):
+    """Base K/V caches and every agent's LR cache from one set of hidden states, fp64.
+
+    [ReBase]: the shared base cache is computed from adapter-free hidden
+    states X with the pretrained projections, K_base = X . W_k and
+    V_base = X . W_v ([LRAgent-1]: the base part of the value cache comes from
+    the frozen pretrained weights; keys carry no adapter term).  [PReCache]:
+    each agent's LR cache L_i = X . A_i is computed in the same pass over X.
+    No rotary embedding or other position encoding is applied here.
+
+    X [n, D]; W_k, W_v [D, Hkv*d]; A_cat [D, A*r].  Returns
+    (K_base [n, Hkv, d], V_base [n, Hkv, d], L [n, A*r]).
+    """
+    X = to_f64(X)
+    n = X.shape[0]
+    K_base = (X @ to_f64(W_k)).reshape(n, hkv, d)
+    V_base = (X @ to_f64(W_v)).reshape(n, hkv, d)
+    L = X @ to_f64(A_cat)
+    return K_base, V_base, L
 
 
 def agent_value_cache(V_base, L_i, B_i, hkv: int, d: int) -> np.ndarray:

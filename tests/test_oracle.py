@@ -10,7 +10,10 @@
 * GQA equals MHA with duplicated kv heads; ragged equals separate requests;
   token permutation invariance; n = 1 returns V_i[0]; O is affine in B;
   each agent's output depends only on its own L_i, B_i;
-* lr_cache_build against hand-derived values and per-agent block structure.
+* lr_cache_build against hand-derived values and per-agent block structure;
+* rebase_kv_lr_build against a hand-derived case, brute-force sums on integer
+  inputs, one-hot hidden states (each output row is a weight row) and the
+  head layout of K_base / V_base.
 """
 import dataclasses
 import glob
@@ -50,6 +53,12 @@ def test_golden_fixture(golden_dir, name):
         O = oracle.prefill(_arr(c["Q"]), _arr(c["K_base"]), _arr(c["V_base"]), _arr(c["L"]),
                            _arr(c["B"]), n0=c["n0"], rank=c["rank"])
         np.testing.assert_allclose(O, _arr(c["O"]), rtol=0, atol=1e-12)
+    elif c["kind"] == "rebase":
+        K, V, L = oracle.rebase_kv_lr_build(_arr(c["X"]), _arr(c["W_k"]), _arr(c["W_v"]), _arr(c["A_cat"]),
+                                            hkv=c["hkv"], d=c["d"])
+        np.testing.assert_array_equal(K, _arr(c["K_base"]))
+        np.testing.assert_array_equal(V, _arr(c["V_base"]))
+        np.testing.assert_array_equal(L, _arr(c["L"]))
     else:
         L = oracle.lr_cache_build(_arr(c["X"]), _arr(c["A_cat"]))
         np.testing.assert_array_equal(L, _arr(c["L"]))
@@ -292,3 +301,48 @@ def test_agent_value_cache_by_brute_force():
     one_hot[:, 1] = 1.0
     picked = oracle.agent_value_cache(np.zeros_like(V), one_hot, B, hkv, d)
     assert np.array_equal(picked[0], B[1].reshape(hkv, d))
+
+
+# ----------------------------------------------------------------------------
+# ReBaseShared base projection fused with the LR build
+# ----------------------------------------------------------------------------
+
+def _int_rebase_inputs(n, D, hkv, d, A, r, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.integers(-3, 4, (n, D)).astype(np.float64), rng.integers(-3, 4, (D, hkv * d)).astype(np.float64),
+            rng.integers(-3, 4, (D, hkv * d)).astype(np.float64), rng.integers(-3, 4, (D, A * r)).astype(np.float64))
+
+
+def test_rebase_projection_by_brute_force():
+    """Every output element is the plain sum over d_model (integer inputs: exact)."""
+    n, D, hkv, d, A, r = 5, 7, 2, 3, 3, 2
+    X, Wk, Wv, Ac = _int_rebase_inputs(n, D, hkv, d, A, r, seed=3)
+    K, V, L = oracle.rebase_kv_lr_build(X, Wk, Wv, Ac, hkv=hkv, d=d)
+    for t in range(n):
+        for h in range(hkv):
+            for j in range(d):
+                c = h * d + j
+                assert K[t, h, j] == sum(X[t, k] * Wk[k, c] for k in range(D))
+                assert V[t, h, j] == sum(X[t, k] * Wv[k, c] for k in range(D))
+        for c in range(A * r):
+            assert L[t, c] == sum(X[t, k] * Ac[k, c] for k in range(D))
+
+
+def test_rebase_projection_one_hot_rows_select_weight_rows():
+    """X = identity: token t's K/V/L rows are row t of W_k, W_v, A_cat (head h = columns [h*d, (h+1)*d))."""
+    D, hkv, d, A, r = 6, 3, 2, 2, 3
+    _, Wk, Wv, Ac = _int_rebase_inputs(1, D, hkv, d, A, r, seed=5)
+    K, V, L = oracle.rebase_kv_lr_build(np.eye(D), Wk, Wv, Ac, hkv=hkv, d=d)
+    for t in range(D):
+        for h in range(hkv):
+            np.testing.assert_array_equal(K[t, h], Wk[t, h * d:(h + 1) * d])
+            np.testing.assert_array_equal(V[t, h], Wv[t, h * d:(h + 1) * d])
+        np.testing.assert_array_equal(L[t], Ac[t])
+
+
+def test_rebase_lr_block_matches_the_lr_build():
+    x = make_build_inputs(9, 64, 2, 8, torch.bfloat16, seed=2)
+    rng = np.random.default_rng(1)
+    Wk, Wv = rng.standard_normal((64, 32)), rng.standard_normal((64, 32))
+    _, _, L = oracle.rebase_kv_lr_build(x["X"], Wk, Wv, x["A_cat"], hkv=2, d=16)
+    np.testing.assert_array_equal(L, oracle.lr_cache_build(x["X"], x["A_cat"]))

@@ -29,6 +29,9 @@ MUTANTS = {
     "softmax_not_normalised": ("w /= w.sum()", "w /= len(w)"),
     "build_blocks_shifted": ("return to_f64(X) @ to_f64(A_cat)",
                              "return to_f64(X) @ np.roll(to_f64(A_cat), 1, axis=1)"),
+    "rebase_k_v_swapped": ("K_base = (X @ to_f64(W_k))", "K_base = (X @ to_f64(W_v))"),
+    "rebase_head_layout_transposed": ("V_base = (X @ to_f64(W_v)).reshape(n, hkv, d)",
+                                      "V_base = (X @ to_f64(W_v)).reshape(n, d, hkv).transpose(0, 2, 1)"),
     "ragged_offset_shift": ("t0, t1 = offs[q_req], offs[q_req + 1]\n        Kq",
                             "t0, t1 = offs[q_req], offs[q_req + 1] + (1 if q_req + 2 < len(offs) else 0)\n        Kq"),
 }
@@ -56,6 +59,11 @@ def _golden_ok(m):
             O = m.prefill(_arr(c["Q"]), _arr(c["K_base"]), _arr(c["V_base"]), _arr(c["L"]),
                           _arr(c["B"]), n0=c["n0"], rank=c["rank"])
             want = _arr(c["O"])
+        elif c["kind"] == "rebase":
+            K, V, L = m.rebase_kv_lr_build(_arr(c["X"]), _arr(c["W_k"]), _arr(c["W_v"]), _arr(c["A_cat"]),
+                                           hkv=c["hkv"], d=c["d"])
+            O = np.concatenate([K.ravel(), V.ravel(), L.ravel()])
+            want = np.concatenate([_arr(c["K_base"]).ravel(), _arr(c["V_base"]).ravel(), _arr(c["L"]).ravel()])
         else:
             O = m.lr_cache_build(_arr(c["X"]), _arr(c["A_cat"]))
             want = _arr(c["L"])
