@@ -2,6 +2,7 @@
 
 Public API (thin wrappers over the C ABI in include/flash_lora_attn.h):
   lr_cache_build(X, A_cat, L=None)          L = X . A_cat for every agent at once
+  rebase_kv_lr_build(X, W_cat, ...)         [K_base | V_base | L] = X . [W_k | W_v | A_cat] in one pass
   flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, rank=...)
   flash_lora_attn_prefill(Q, K_base, V_base, L, B, n0, rank=...)
   PreparedDecode(...)                       a decode call marshalled once, one C call per step
@@ -27,6 +28,7 @@ from .binding import (  # noqa: F401
     load_library,
     lora_value_expand,
     lr_cache_build,
+    rebase_kv_lr_build,
     version,
 )
 

@@ -28,7 +28,7 @@ STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "F
 EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
             "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
             "fla_last_error", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc",
-            "lora_value_expand", "flash_lora_attn_decode_host_io")
+            "lora_value_expand", "flash_lora_attn_decode_host_io", "rebase_kv_lr_build")
 
 
 class FlaError(RuntimeError):
@@ -62,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         dims_p = ctypes.POINTER(AttnDims)
         lib.lr_cache_build.argtypes = [vp, i64, vp, vp, i64, i64, i32, i32, i32, i32, i32, vp]
         lib.lr_cache_build.restype = ctypes.c_int
+        lib.rebase_kv_lr_build.argtypes = [vp, i64, vp, vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, i32, i32, vp]
+        lib.rebase_kv_lr_build.restype = ctypes.c_int
         lib.flash_lora_attn_decode_workspace_size.argtypes = [dims_p, i32, i64]
         lib.flash_lora_attn_decode_workspace_size.restype = sz
         lib.flash_lora_attn_decode.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, i32, i64, vp, vp, sz, vp]
@@ -168,6 +170,42 @@ def lr_cache_build(X: torch.Tensor, A_cat: torch.Tensor, L: Optional[torch.Tenso
     _check(lib.lr_cache_build(X.data_ptr(), X.stride(0), A_cat.data_ptr(), L.data_ptr(), L.stride(0), n, D,
                               n_agents, N // n_agents, _dtype_code(X), KERNELS[kernel], _stream_ptr(stream)))
     return L
+
+
+def rebase_kv_lr_build(X: torch.Tensor, W_cat: torch.Tensor, *, hkv: int, head_dim: int, n_agents: int,
+                       rank: int, K_base: Optional[torch.Tensor] = None, V_base: Optional[torch.Tensor] = None,
+                       L: Optional[torch.Tensor] = None, kernel: str = "auto", stream=None):
+    """[K_base | V_base | L] = X . [W_k | W_v | A_cat] in one pass over X.
+
+    X [n, D] (rows may be strided); W_cat [D, 2*hkv*head_dim + n_agents*rank]
+    contiguous; K_base, V_base [n, hkv, head_dim] contiguous; L [n, A*r] with
+    unit column stride.  Returns (K_base, V_base, L).
+    """
+    lib = load_library()
+    _need_cuda(X, W_cat, K_base, V_base, L)
+    n, D = X.shape
+    kv, lr = hkv * head_dim, n_agents * rank
+    if tuple(W_cat.shape) != (D, 2 * kv + lr):
+        raise ValueError("W_cat must be [d_model, 2*hkv*head_dim + n_agents*rank]")
+    _dense(W_cat, "W_cat")
+    if K_base is None:
+        K_base = torch.empty((n, hkv, head_dim), dtype=X.dtype, device=X.device)
+    if V_base is None:
+        V_base = torch.empty((n, hkv, head_dim), dtype=X.dtype, device=X.device)
+    if L is None:
+        L = torch.empty((n, lr), dtype=X.dtype, device=X.device)
+    for t, nm in ((K_base, "K_base"), (V_base, "V_base")):
+        _dense(t, nm)
+        if tuple(t.shape) != (n, hkv, head_dim):
+            raise ValueError(f"{nm} must be [n_tokens, hkv, head_dim]")
+    if X.stride(1) != 1 or L.stride(1) != 1 or tuple(L.shape) != (n, lr):
+        raise ValueError("X and L need unit column stride; L must be [n_tokens, n_agents*rank]")
+    if not (X.dtype == W_cat.dtype == K_base.dtype == V_base.dtype == L.dtype):
+        raise TypeError("X, W_cat and the outputs must share one dtype")
+    _check(lib.rebase_kv_lr_build(X.data_ptr(), X.stride(0), W_cat.data_ptr(), K_base.data_ptr(), V_base.data_ptr(),
+                                  L.data_ptr(), L.stride(0), n, D, hkv, head_dim, n_agents, rank, _dtype_code(X),
+                                  KERNELS[kernel], _stream_ptr(stream)))
+    return K_base, V_base, L
 
 
 def flash_lora_attn_decode(Q, K_base, V_base, L, B, offsets, *, rank: int,

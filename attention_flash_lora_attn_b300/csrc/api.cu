@@ -75,6 +75,43 @@ fla_status check_dims(const fla_attn_dims *d, float *scale) {
   return FLA_OK;
 }
 
+// out = X . W over the column segments seg[0..n_seg) of W (row-major, the
+// segments' columns side by side): the tcgen05 GEMM reads each tile of X once
+// for every segment; the CUDA-core fallback runs one launch per segment.
+fla_status run_projection(const char *what, const void *X, int64_t ldx, const void *W, const fla::BuildSegment *seg,
+                          int n_seg, int64_t n_tokens, int32_t d_model, int32_t dtype, int32_t kernel,
+                          cudaStream_t s) {
+  if (kernel == FLA_KERNEL_MMA_SYNC)
+    return fail(FLA_ERR_UNSUPPORTED, "%s has no mma.sync kernel (use TENSOR or TCGEN05)", what);
+  const bool tc_ok = fla::build_tc_supported(X, ldx, W, seg, n_seg, d_model, dtype);
+  if ((kernel == FLA_KERNEL_TENSOR || kernel == FLA_KERNEL_TCGEN05) && !tc_ok)
+    return fail(FLA_ERR_UNSUPPORTED, "%s: shape/alignment outside the tensor-core kernel (needs bf16, "
+                "d_model %% 64 == 0, every output width %% 32 == 0, 16-byte alignment, row strides multiples of 8)",
+                what);
+  if (tc_ok && kernel != FLA_KERNEL_SIMT) {
+    const fla_status st = fla::build_tc_launch(X, ldx, W, seg, n_seg, n_tokens, d_model, s);
+    if (st != FLA_OK) return fail(st, "%s (tensor): %s", what, fla::build_tc_last_error());
+    return check_launch(what);
+  }
+  int64_t lda = 0;
+  for (int i = 0; i < n_seg; ++i) lda += seg[i].cols;
+  const size_t esize = dtype == FLA_F32 ? 4 : 2;
+  int64_t col = 0;
+  for (int i = 0; i < n_seg; ++i) {
+    fla::SimtBuildParams p{X, static_cast<const uint8_t *>(W) + col * esize, seg[i].ptr, ldx, seg[i].ld,
+                           n_tokens, d_model, seg[i].cols, lda};
+    col += seg[i].cols;
+    if ((n_tokens + 63) / 64 > 0x7fffffffLL || (seg[i].cols + 63) / 64 > 65535)
+      return fail(FLA_ERR_UNSUPPORTED, "%s: n_tokens or the output width too large", what);
+    dim3 grid((unsigned)((n_tokens + 63) / 64), (unsigned)((seg[i].cols + 63) / 64));
+    if (dtype == FLA_F32)
+      fla::simt_build_kernel<float><<<grid, 256, 0, s>>>(p);
+    else
+      fla::simt_build_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  }
+  return check_launch(what);
+}
+
 template <typename T>
 void launch_simt_attn(const fla::SimtAttnParams &p, int64_t rows, cudaStream_t s) {
   fla::simt_attn_kernel<T><<<(unsigned)rows, fla::kSimtWarps * 32, 0, s>>>(p);
@@ -132,27 +169,32 @@ fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_cat, void *L
   if (!X || !A_cat || !L) return fail(FLA_ERR_INVALID_ARG, "X, A_cat and L must be non-NULL");
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-  if (kernel == FLA_KERNEL_MMA_SYNC)
-    return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build has no mma.sync kernel (use TENSOR or TCGEN05)");
-  const bool tc_ok = fla::build_tc_supported(X, ldx, A_cat, L, ldl, d_model, n_cols, dtype);
-  if ((kernel == FLA_KERNEL_TENSOR || kernel == FLA_KERNEL_TCGEN05) && !tc_ok)
-    return fail(FLA_ERR_UNSUPPORTED, "lr_cache_build: shape/alignment outside the tensor-core kernel "
-                "(needs bf16, d_model %% 64 == 0, n_agents * rank %% 32 == 0, 16-byte alignment, "
-                "ldx and ldl multiples of 8)");
-  if (tc_ok && kernel != FLA_KERNEL_SIMT) {
-    fla_status st = fla::build_tc_launch(X, ldx, A_cat, L, ldl, n_tokens, d_model, n_cols, s);
-    if (st != FLA_OK) return fail(st, "lr_cache_build (tensor): %s", fla::build_tc_last_error());
-    return check_launch("lr_cache_build (tensor)");
-  }
-  fla::SimtBuildParams p{X, A_cat, L, ldx, ldl, n_tokens, d_model, n_cols};
-  dim3 grid((unsigned)((n_tokens + 63) / 64), (unsigned)((n_cols + 63) / 64));
-  if ((n_tokens + 63) / 64 > 0x7fffffffLL || (n_cols + 63) / 64 > 65535)
-    return fail(FLA_ERR_UNSUPPORTED, "n_tokens or n_agents * rank too large");
-  if (dtype == FLA_F32)
-    fla::simt_build_kernel<float><<<grid, 256, 0, s>>>(p);
-  else
-    fla::simt_build_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
-  return check_launch("lr_cache_build (simt)");
+  const fla::BuildSegment seg{L, ldl, n_cols};
+  return run_projection("lr_cache_build", X, ldx, A_cat, &seg, 1, n_tokens, d_model, dtype, kernel, s);
+}
+
+// ---------------------------------------------------------------------------
+fla_status rebase_kv_lr_build(const void *X, int64_t ldx, const void *W_cat, void *K_base, void *V_base, void *L,
+                              int64_t ldl, int64_t n_tokens, int32_t d_model, int32_t hkv, int32_t head_dim,
+                              int32_t n_agents, int32_t rank, int32_t dtype, int32_t kernel, fla_stream_t stream) {
+  g_last_error.clear();
+  if (n_tokens < 0 || d_model < 1 || hkv < 1 || head_dim < 1 || n_agents < 1 || rank < 1)
+    return fail(FLA_ERR_INVALID_ARG, "n_tokens must be >= 0; d_model, hkv, head_dim, n_agents and rank >= 1");
+  const int64_t kv64 = (int64_t)hkv * head_dim, lr64 = (int64_t)n_agents * rank;
+  if (2 * kv64 + lr64 > INT32_MAX) return fail(FLA_ERR_INVALID_ARG, "the projection width overflows int32");
+  if (dtype != FLA_F32 && dtype != FLA_BF16) return fail(FLA_ERR_INVALID_ARG, "bad dtype %d", dtype);
+  if (kernel < FLA_KERNEL_AUTO || kernel > FLA_KERNEL_TCGEN05)
+    return fail(FLA_ERR_INVALID_ARG, "kernel %d is not a fla_kernel", kernel);
+  if (ldx < d_model) return fail(FLA_ERR_INVALID_ARG, "ldx (%lld) < d_model (%d)", (long long)ldx, d_model);
+  if (ldl < lr64)
+    return fail(FLA_ERR_INVALID_ARG, "ldl (%lld) < n_agents * rank (%lld)", (long long)ldl, (long long)lr64);
+  if (n_tokens == 0) return ok();
+  if (!X || !W_cat || !K_base || !V_base || !L)
+    return fail(FLA_ERR_INVALID_ARG, "X, W_cat, K_base, V_base and L must be non-NULL");
+  const fla::BuildSegment seg[3] = {{K_base, kv64, (int32_t)kv64}, {V_base, kv64, (int32_t)kv64},
+                                    {L, ldl, (int32_t)lr64}};
+  return run_projection("rebase_kv_lr_build", X, ldx, W_cat, seg, 3, n_tokens, d_model, dtype, kernel,
+                        reinterpret_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

@@ -24,9 +24,9 @@
 // Short inputs (a few row tiles) would leave most SMs idle, so the plan may
 // split d_model over a thread-block cluster of S CTAs: each accumulates its
 // share of the k-steps, writes its fp32 partial tile into its own shared
-// memory, and CTA j of the cluster sums rows [j*128/S, (j+1)*128/S) of all S
-// partials through distributed shared memory in rank order (deterministic)
-// and stores them as bf16.
+// memory, and after a cluster barrier CTA j of the cluster sums rows
+// [j*128/S, (j+1)*128/S) of all S partials through distributed shared memory
+// in rank order (deterministic) and stores them as bf16.
 // Every wait is bounded; on a timeout the CTA records the error, waits
 // (bounded) for its copies and MMAs in flight, frees TMEM and returns.
 #pragma once
@@ -49,15 +49,20 @@ constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxSplit = 16;
 constexpr int kMaxTileCols = 512;        // TMEM columns
 
+constexpr int kMaxSegments = 3;
+
+// Columns [seg_begin(s), seg_end[s]) of the product go to out[s] (row stride
+// ld[s], column 0 = the segment's first column); segment ends are multiples of 32.
 struct Params {
-  __nv_bfloat16 *L;
-  int64_t ldl, n;
+  __nv_bfloat16 *out[kMaxSegments];
+  int64_t ld[kMaxSegments];
+  int32_t seg_end[kMaxSegments];
+  int32_t n_seg;
+  int64_t n;
   int32_t K;                 // d_model
-  int32_t N;                 // columns of L (A * r)
-  int32_t n_tile;            // columns per CTA (multiple of 64)
+  int32_t N;                 // columns of the product (= seg_end[n_seg - 1])
+  int32_t tile_boxes;        // 64-column boxes per column tile (<= 8)
   int32_t n_ntiles;          // column tiles
-  int32_t n_chunks;          // MMAs per k16 step (each <= 256 columns)
-  int32_t chunk_boxes[2];    // 64-column boxes per MMA chunk
   int32_t stages;
   int32_t split;             // CTAs per cluster along d_model (1: no split)
   int32_t ksteps;            // k-steps per CTA
@@ -65,15 +70,26 @@ struct Params {
   uint32_t tmem_cols;
 };
 
+// Destination of 4 (or more, within one segment) consecutive product columns
+// starting at column c of row `row`.
+__device__ __forceinline__ __nv_bfloat16 *out_ptr(const Params &p, int64_t row, int c) {
+  // constant indices only, so the parameter arrays stay in the constant bank
+  const bool s1 = p.n_seg > 1 && c >= p.seg_end[0];
+  const bool s2 = p.n_seg > 2 && c >= p.seg_end[1];
+  __nv_bfloat16 *base = s2 ? p.out[2] : (s1 ? p.out[1] : p.out[0]);
+  const int64_t ld = s2 ? p.ld[2] : (s1 ? p.ld[1] : p.ld[0]);
+  const int begin = s2 ? p.seg_end[1] : (s1 ? p.seg_end[0] : 0);
+  return base + row * ld + (c - begin);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int n_boxes = p.n_tile / kBoxN;
   const int a_bytes = kBM * kBK * 2;
-  const int stage_bytes = a_bytes + n_boxes * kBoxBytes;
+  const int stage_bytes = a_bytes + p.tile_boxes * kBoxBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
-  // bars: full[stages] | empty[stages] | acc_full | drain | red_ready | red_done
+  // bars: full[stages] | empty[stages] | acc_full | drain
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -81,15 +97,19 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   const int kslice = blockIdx.x % p.split;  // = rank in the cluster (cluster dims (split, 1, 1))
   const int nt = (int)(tile % p.n_ntiles);
   const int64_t m0 = (tile / p.n_ntiles) * kBM;
-  const int c0 = nt * p.n_tile;             // first column of L this CTA produces
+  const int c0 = nt * p.tile_boxes * kBoxN;  // first product column of this CTA
+  // boxes of this tile (the last tile may be narrower), split into <= 2 MMA
+  // chunks of <= 4 boxes (256 columns)
+  const int n_boxes = min(p.tile_boxes, ((p.N + kBoxN - 1) / kBoxN) - nt * p.tile_boxes);
+  const int chunk0 = n_boxes <= 4 ? n_boxes : (n_boxes + 1) / 2;
+  const int chunk1 = n_boxes - chunk0;
+  const int load_bytes = a_bytes + n_boxes * kBoxBytes;
   const int n_k = p.ksteps;
   const int kt0 = kslice * p.ksteps;
   const uint32_t full0 = ptx::smem_u32(&bars[0]);
   const uint32_t empty0 = ptx::smem_u32(&bars[p.stages]);
   const uint32_t acc_full = ptx::smem_u32(&bars[2 * p.stages]);
   const uint32_t drain = ptx::smem_u32(&bars[2 * p.stages + 1]);
-  const uint32_t red_ready = ptx::smem_u32(&bars[2 * p.stages + 2]);
-  const uint32_t red_done = ptx::smem_u32(&bars[2 * p.stages + 3]);
 
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -99,8 +119,6 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     }
     ptx::mbar_init(acc_full, 1);
     ptx::mbar_init(drain, 1);
-    ptx::mbar_init(red_ready, p.split);  // one arrival per CTA of the cluster
-    ptx::mbar_init(red_done, p.split);
     ptx::fence_mbar_init();
   }
   if (warp == 1) {
@@ -110,9 +128,6 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  // peers arrive on this CTA's barriers later: their initialisation must be
-  // visible cluster-wide first (every CTA of a cluster is co-resident)
-  if (p.split > 1) ptx::cluster_sync_all();
   const uint32_t tmem = s_tmem;
 
   if (warp == 0) {
@@ -130,7 +145,7 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
         }
         if (*(volatile int *)&s_abort) break;
         const uint32_t fb = full0 + 8 * s;
-        ptx::mbar_arrive_expect_tx(fb, stage_bytes);
+        ptx::mbar_arrive_expect_tx(fb, load_bytes);
         const uint32_t sa = ptx::smem_u32(smem + s * stage_bytes);
         const int k = (kt0 + kt) * kBK;
         ptx::tma_load_2d(sa, &tmX, k, (int32_t)m0, fb);
@@ -149,8 +164,8 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   } else if (warp == 1) {
     // ======================= MMA issuer =======================
     if (lane == 0) {
-      const uint32_t idesc0 = ptx::idesc_bf16_f32(kBM, p.chunk_boxes[0] * kBoxN) | (1u << 16);  // B MN-major
-      const uint32_t idesc1 = ptx::idesc_bf16_f32(kBM, p.chunk_boxes[1] * kBoxN) | (1u << 16);
+      const uint32_t idesc0 = ptx::idesc_bf16_f32(kBM, chunk0 * kBoxN) | (1u << 16);  // B MN-major
+      const uint32_t idesc1 = ptx::idesc_bf16_f32(kBM, (chunk1 > 0 ? chunk1 : 1) * kBoxN) | (1u << 16);
       const uint64_t d_a = ptx::smem_desc_k128(ptx::smem_u32(smem));
       const uint64_t d_b = ptx::smem_desc_mn128(ptx::smem_u32(smem) + a_bytes, kBoxBytes);
       bool ok = true;
@@ -171,9 +186,9 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
           // A: 16 K-columns = 32 bytes further along each swizzled row;
           // B: 16 K-rows = two 1024-byte swizzle atoms further on
           ptx::tc_mma_f16(tmem, ptx::desc_advance(da, k16 * 32), ptx::desc_advance(db, k16 * 2048), idesc0, acc);
-          if (p.n_chunks > 1)
-            ptx::tc_mma_f16(tmem + p.chunk_boxes[0] * kBoxN, ptx::desc_advance(da, k16 * 32),
-                            ptx::desc_advance(db, p.chunk_boxes[0] * kBoxBytes + k16 * 2048), idesc1, acc);
+          if (chunk1 > 0)
+            ptx::tc_mma_f16(tmem + chunk0 * kBoxN, ptx::desc_advance(da, k16 * 32),
+                            ptx::desc_advance(db, chunk0 * kBoxBytes + k16 * 2048), idesc1, acc);
         }
         ptx::tc_commit(empty0 + 8 * s);  // stage s is free once these MMAs have read it
       }
@@ -202,7 +217,7 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
     if (ready) {
       ptx::tc_fence_after();
       const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-      const int ncols = min(p.n_tile, p.N - c0);  // multiple of 32
+      const int ncols = min(p.tile_boxes * kBoxN, p.N - c0);  // multiple of 32
       // split-K: the fp32 partial goes to this CTA's own shared memory (the
       // stage ring is idle: every MMA, hence every copy, has completed)
       float *red = reinterpret_cast<float *>(smem) + (size_t)rloc * p.red_pitch;
@@ -222,7 +237,7 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             o[i] = ptx::pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-          uint4 *dst = reinterpret_cast<uint4 *>(p.L + row * p.ldl + c0 + c);
+          uint4 *dst = reinterpret_cast<uint4 *>(out_ptr(p, row, c0 + c));  // 32 columns, one segment
 #pragma unroll
           for (int i = 0; i < 4; ++i) dst[i] = out[i];
         }
@@ -235,43 +250,42 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   if (p.split == 1) return;
 
   // ======================= split-K: sum the cluster's partial tiles =======================
-  const uint32_t rank = (uint32_t)kslice;
-  if (threadIdx.x == 0 && !*(volatile int *)&s_abort) {
-    ptx::fence_acq_rel_cluster();  // this CTA's partial (written before the barrier above) first
-    for (int s = 0; s < p.split; ++s) ptx::mbar_arrive_cluster(ptx::mapa_cluster(red_ready, (uint32_t)s));
-  }
-  // every CTA's partial is complete once all of them have arrived here; an
-  // aborted peer never arrives and this wait runs out instead
-  const bool have_all = !*(volatile int *)&s_abort && ptx::mbar_wait_cluster(red_ready, 0);
-  if (!have_all && threadIdx.x == 0 && !*(volatile int *)&s_abort) set_device_error(kErrBuildClusterWait);
-  if (have_all) {
+  // Two cluster barriers, each reached by every thread of every CTA of the
+  // cluster exactly once and only through bounded waits: the first publishes
+  // the partial tiles (release / acquire at cluster scope), the second keeps
+  // each CTA's shared memory alive until every peer has read it.  A CTA that
+  // aborted still takes part (its error is recorded; the outputs are then
+  // undefined).
+  ptx::cluster_sync_all();
+  {
     const int rows = kBM / p.split;
-    const int r0 = (int)rank * rows;
-    const int ncols = min(p.n_tile, p.N - c0);
+    const int r0 = kslice * rows;
+    const int ncols = min(p.tile_boxes * kBoxN, p.N - c0);
     const int c4n = ncols / 4;
     const uint32_t red_local = ptx::smem_u32(smem);
     for (int e = threadIdx.x; e < rows * c4n; e += kThreads) {
       const int rr = e / c4n, c4 = e - rr * c4n;
       const int rloc = r0 + rr;
       const uint32_t off = (uint32_t)(rloc * p.red_pitch + c4 * 4) * 4u;
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int s = 0; s < p.split; ++s) {  // rank order: the same sum whichever CTA finishes first
-        const float4 v = ptx::ld_cluster_f4(ptx::mapa_cluster(red_local + off, (uint32_t)s));
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
+      // every peer's load in flight at once, then the sum in rank order (the
+      // same result whichever CTA finished first)
+      float4 v[kMaxSplit];
+#pragma unroll
+      for (int q = 0; q < kMaxSplit; ++q)
+        if (q < p.split) v[q] = ptx::ld_cluster_f4(ptx::mapa_cluster(red_local + off, (uint32_t)q));
+      float4 acc = v[0];
+#pragma unroll
+      for (int q = 1; q < kMaxSplit; ++q)
+        if (q < p.split) {
+          acc.x += v[q].x; acc.y += v[q].y; acc.z += v[q].z; acc.w += v[q].w;
+        }
       const int64_t row = m0 + rloc;
       if (row < p.n)
-        *reinterpret_cast<uint2 *>(p.L + row * p.ldl + c0 + c4 * 4) =
+        *reinterpret_cast<uint2 *>(out_ptr(p, row, c0 + c4 * 4)) =
             make_uint2(ptx::pack_bf16(acc.x, acc.y), ptx::pack_bf16(acc.z, acc.w));
     }
   }
-  __syncthreads();
-  // this CTA's partial must stay in place until every peer has read it
-  if (threadIdx.x == 0) {
-    if (have_all)
-      for (int s = 0; s < p.split; ++s) ptx::mbar_arrive_cluster(ptx::mapa_cluster(red_done, (uint32_t)s));
-    if (!ptx::mbar_wait_cluster(red_done, 0)) set_device_error(kErrBuildClusterWait);
-  }
+  ptx::cluster_sync_all();
 }
 
 }  // namespace bld
@@ -286,83 +300,89 @@ inline const char *&build_tc_err() {
 inline const char *build_tc_last_error() { return build_tc_err(); }
 
 struct BuildPlan {
-  int n_tile, n_ntiles, n_chunks, chunk_boxes[2];
-  int stages, smem_bytes, split, ksteps, red_pitch;
+  int tile_boxes, n_ntiles, stages, smem_bytes, split, ksteps, red_pitch;
   uint32_t tmem_cols;
   bool ok;
 };
 
-// Shape part of the plan (independent of the number of rows).
-inline BuildPlan build_tc_shape_plan(int d_model, int n_cols) {
+inline int build_smem_bytes(int stages, int stage) { return stages * stage + (2 * stages + 2) * 8 + 1024; }
+
+// Plan for column tiles of `bpt` boxes (64 columns each) and a split of d_model
+// over `split` CTAs; ok = false when it does not fit shared memory.
+inline BuildPlan build_tc_plan_for(int d_model, int n_cols, int bpt, int split) {
   BuildPlan pl{};
   pl.ok = false;
-  if (d_model < bld::kBK || d_model % bld::kBK != 0 || n_cols % 32 != 0 || n_cols < 32) return pl;
-  pl.n_ntiles = (n_cols + bld::kMaxTileCols - 1) / bld::kMaxTileCols;
-  const int per = (n_cols + pl.n_ntiles - 1) / pl.n_ntiles;
-  pl.n_tile = (per + bld::kBoxN - 1) / bld::kBoxN * bld::kBoxN;
-  const int boxes = pl.n_tile / bld::kBoxN;
-  pl.n_chunks = (boxes + 3) / 4;  // <= 256 columns per MMA
-  pl.chunk_boxes[0] = (boxes + pl.n_chunks - 1) / pl.n_chunks;
-  pl.chunk_boxes[1] = boxes - pl.chunk_boxes[0];
-  if (pl.n_chunks > 2 || pl.chunk_boxes[0] > 4 || pl.chunk_boxes[1] > 4) return pl;
-  if (pl.n_chunks == 1) pl.chunk_boxes[1] = pl.chunk_boxes[0];  // unused, keeps the descriptor valid
-  const int stage = bld::kBM * bld::kBK * 2 + boxes * bld::kBoxBytes;
-  int stages = (bld::kSmemBudget - 1024 - 64) / stage;
-  if (stages > 8) stages = 8;
-  if (stages < 2) return pl;
-  pl.stages = stages;
+  const int boxes = (n_cols + bld::kBoxN - 1) / bld::kBoxN;
+  const int nk = d_model / bld::kBK;
+  if (bpt < 1 || bpt > 8 || nk % split != 0) return pl;
+  pl.tile_boxes = std::min(bpt, boxes);
+  pl.n_ntiles = (boxes + pl.tile_boxes - 1) / pl.tile_boxes;
+  pl.split = split;
+  pl.ksteps = nk / split;
+  pl.red_pitch = pl.tile_boxes * bld::kBoxN + 4;
+  const int stage = bld::kBM * bld::kBK * 2 + pl.tile_boxes * bld::kBoxBytes;
+  int st = (bld::kSmemBudget - 1024 - 128) / stage;
+  st = std::min(st, 8);
+  if (split > 1) {
+    // no more stages than k-steps, but room for the fp32 partial tile
+    st = std::min(st, std::max(2, pl.ksteps));
+    while (st * stage < bld::kBM * pl.red_pitch * 4) ++st;
+  }
+  if (st < 2 || build_smem_bytes(st, stage) > 227 * 1024) return pl;
+  pl.stages = st;
+  pl.smem_bytes = build_smem_bytes(st, stage);
   uint32_t cols = 32;
-  while ((int)cols < pl.n_tile) cols <<= 1;
+  while ((int)cols < pl.tile_boxes * bld::kBoxN) cols <<= 1;
   pl.tmem_cols = cols;
-  pl.split = 1;
-  pl.ksteps = d_model / bld::kBK;
-  pl.red_pitch = pl.n_tile + 4;
-  pl.smem_bytes = stages * stage + 6 * 8 + (2 * stages) * 8 + 1024;
   pl.ok = true;
   return pl;
 }
 
-// Full plan for n rows on `sms` SMs: when the tiles cover less than half the
-// GPU, d_model is split over a cluster of up to max_split CTAs (k-steps divide
-// evenly; the fp32 partial tile must fit the stage ring).
-inline BuildPlan build_tc_plan(int64_t n, int d_model, int n_cols, int sms, int max_split) {
-  BuildPlan pl = build_tc_shape_plan(d_model, n_cols);
-  if (!pl.ok || n <= 0) return pl;
-  const int64_t tiles = (n + bld::kBM - 1) / bld::kBM * pl.n_ntiles;
-  const int nk = d_model / bld::kBK;
-  const int stage = bld::kBM * bld::kBK * 2 + (pl.n_tile / bld::kBoxN) * bld::kBoxBytes;
-  const int red_bytes = bld::kBM * pl.red_pitch * 4;
-  if (tiles * 2 <= sms) {
-    for (int s = max_split; s >= 2; s >>= 1) {
-      if (tiles * s > sms || nk % s != 0) continue;
-      int st = std::min(8, std::max(2, nk / s));  // no more stages than k-steps
-      while (st * stage < red_bytes) ++st;
-      if (st * stage + 6 * 8 + 2 * st * 8 + 1024 > 227 * 1024) continue;
-      pl.split = s;
-      pl.ksteps = nk / s;
-      pl.stages = st;
-      pl.smem_bytes = st * stage + 6 * 8 + 2 * st * 8 + 1024;
-      break;
-    }
-  }
-  return pl;
+// Widest balanced tiles (<= 8 boxes = 512 TMEM columns), no split.
+inline BuildPlan build_tc_shape_plan(int d_model, int n_cols) {
+  BuildPlan pl{};
+  pl.ok = false;
+  if (d_model < bld::kBK || d_model % bld::kBK != 0 || n_cols % 32 != 0 || n_cols < 32) return pl;
+  const int boxes = (n_cols + bld::kBoxN - 1) / bld::kBoxN;
+  const int nt = (boxes + 7) / 8;
+  return build_tc_plan_for(d_model, n_cols, (boxes + nt - 1) / nt, 1);
 }
 
-inline bool build_tc_supported(const void *X, int64_t ldx, const void *A_cat, const void *L, int64_t ldl,
-                               int d_model, int n_cols, int dtype) {
-  auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
-  return dtype == FLA_BF16 && al16(X) && al16(A_cat) && al16(L) && ldx % 8 == 0 && ldl % 8 == 0 &&
-         build_tc_shape_plan(d_model, n_cols).ok;
+// Full plan for n rows on `sms` SMs.  When the widest tiles cover less than
+// half the GPU, narrower tiles (<= 4 boxes) and a split of d_model over a
+// cluster of up to max_split CTAs are considered; the plan that puts the
+// most CTAs on the SMs (at most one wave) wins, the larger split on ties.
+inline BuildPlan build_tc_plan(int64_t n, int d_model, int n_cols, int sms, int max_split) {
+  BuildPlan best = build_tc_shape_plan(d_model, n_cols);
+  if (!best.ok || n <= 0) return best;
+  const int64_t m_tiles = (n + bld::kBM - 1) / bld::kBM;
+  if (m_tiles * best.n_ntiles * 2 > sms) return best;
+  const int boxes = (n_cols + bld::kBoxN - 1) / bld::kBoxN;
+  int64_t best_ctas = m_tiles * best.n_ntiles;
+  const int narrow_nt = (boxes + 3) / 4;
+  const int bpts[2] = {best.tile_boxes, (boxes + narrow_nt - 1) / narrow_nt};
+  for (int bpt : bpts)
+    for (int sp = max_split; sp >= 2; sp >>= 1) {
+      const BuildPlan c = build_tc_plan_for(d_model, n_cols, bpt, sp);
+      if (!c.ok) continue;
+      const int64_t ctas = m_tiles * c.n_ntiles * sp;
+      if (ctas > sms) continue;
+      if (ctas > best_ctas) {
+        best = c;
+        best_ctas = ctas;
+      }
+    }
+  return best;
 }
 
 // Largest cluster (16, else 8) of this kernel that the device can place with
 // `smem` bytes per CTA; cached per device and shared-memory size.
 inline int build_max_cluster(int smem) {
   static std::mutex mu;
-  static int cached_dev[kMaxDevices], cached_smem[kMaxDevices], cached_val[kMaxDevices];
+  static int cached_smem[kMaxDevices], cached_val[kMaxDevices];
   const int dev = current_device();
   std::lock_guard<std::mutex> lock(mu);
-  if (cached_smem[dev] == smem && cached_val[dev] > 0 && cached_dev[dev] == dev + 1) return cached_val[dev];
+  if (cached_val[dev] > 0 && cached_smem[dev] == smem) return cached_val[dev];
   int best = 8;
   const void *fn = reinterpret_cast<const void *>(bld::build_tc_kernel);
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess &&
@@ -378,25 +398,49 @@ inline int build_max_cluster(int smem) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, bld::build_tc_kernel, &cfg) == cudaSuccess && n >= 1) best = 16;
+    int nclu = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclu, bld::build_tc_kernel, &cfg) == cudaSuccess && nclu >= 1) best = 16;
   }
   cudaGetLastError();  // a refused query leaves no sticky error
-  cached_dev[dev] = dev + 1;
   cached_smem[dev] = smem;
   cached_val[dev] = best;
   return best;
 }
 
-inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *A_cat, void *L, int64_t ldl, int64_t n,
-                                  int d_model, int n_cols, cudaStream_t s) {
-  BuildPlan pl = build_tc_plan(n, d_model, n_cols, device_sm_count(), 8);
+// One output segment of the product: `cols` columns written to `ptr` with row stride `ld`.
+struct BuildSegment {
+  void *ptr;
+  int64_t ld;
+  int32_t cols;
+};
+
+inline bool build_tc_supported(const void *X, int64_t ldx, const void *W, const BuildSegment *seg, int n_seg,
+                               int d_model, int dtype) {
+  auto al16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+  if (dtype != FLA_BF16 || !al16(X) || !al16(W) || ldx % 8 != 0 || n_seg < 1 || n_seg > bld::kMaxSegments)
+    return false;
+  int n_cols = 0;
+  for (int i = 0; i < n_seg; ++i) {
+    if (!al16(seg[i].ptr) || seg[i].ld % 8 != 0 || seg[i].cols % 32 != 0 || seg[i].cols < 32) return false;
+    n_cols += seg[i].cols;
+  }
+  return build_tc_shape_plan(d_model, n_cols).ok;
+}
+
+// out = X . W, W = [d_model rows, sum of the segments' columns], dense row-major,
+// the product's columns written segment by segment.
+inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *W, const BuildSegment *seg, int n_seg,
+                                  int64_t n, int d_model, cudaStream_t s) {
+  int n_cols = 0;
+  for (int i = 0; i < n_seg; ++i) n_cols += seg[i].cols;
+  const int sms = device_sm_count();
+  BuildPlan pl = build_tc_plan(n, d_model, n_cols, sms, 8);
   if (!pl.ok) {
     build_tc_err() = "shape outside the tensor-core build kernel";
     return FLA_ERR_UNSUPPORTED;
   }
-  if (pl.split == 8) {  // try a 16-CTA cluster where the device can place one
-    const BuildPlan p16 = build_tc_plan(n, d_model, n_cols, device_sm_count(), 16);
+  {  // a 16-CTA cluster where the device can place one and it covers more SMs
+    const BuildPlan p16 = build_tc_plan(n, d_model, n_cols, sms, 16);
     if (p16.split == 16 && build_max_cluster(p16.smem_bytes) >= 16) pl = p16;
   }
   PFN_encodeTiled enc = get_encode_tiled();
@@ -404,7 +448,7 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *A_cat,
     build_tc_err() = "cuTensorMapEncodeTiled is not available from the driver";
     return FLA_ERR_CUDA;
   }
-  CUtensorMap mX, mA;
+  CUtensorMap mX, mW;
   const cuuint32_t es[2] = {1, 1};
   {
     const cuuint64_t dims[2] = {(cuuint64_t)d_model, (cuuint64_t)n};
@@ -418,28 +462,31 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *A_cat,
     }
   }
   {
-    // A_cat [d_model rows, n_cols columns], row-major: boxes of 64 columns x 64 rows
+    // W [d_model rows, n_cols columns], row-major: boxes of 64 columns x 64 rows
     const cuuint64_t dims[2] = {(cuuint64_t)n_cols, (cuuint64_t)d_model};
     const cuuint64_t strides[1] = {(cuuint64_t)n_cols * 2};
     const cuuint32_t box[2] = {(cuuint32_t)bld::kBoxN, (cuuint32_t)bld::kBK};
-    if (enc(&mA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(A_cat), dims, strides, box, es,
+    if (enc(&mW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(W), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS) {
-      build_tc_err() = "encoding the A_cat tensor map failed";
+      build_tc_err() = "encoding the weight tensor map failed";
       return FLA_ERR_CUDA;
     }
   }
   bld::Params prm{};
-  prm.L = reinterpret_cast<__nv_bfloat16 *>(L);
-  prm.ldl = ldl;
+  int end = 0;
+  for (int i = 0; i < n_seg; ++i) {
+    prm.out[i] = reinterpret_cast<__nv_bfloat16 *>(seg[i].ptr);
+    prm.ld[i] = seg[i].ld;
+    end += seg[i].cols;
+    prm.seg_end[i] = end;
+  }
+  prm.n_seg = n_seg;
   prm.n = n;
   prm.K = d_model;
   prm.N = n_cols;
-  prm.n_tile = pl.n_tile;
+  prm.tile_boxes = pl.tile_boxes;
   prm.n_ntiles = pl.n_ntiles;
-  prm.n_chunks = pl.n_chunks;
-  prm.chunk_boxes[0] = pl.chunk_boxes[0];
-  prm.chunk_boxes[1] = pl.chunk_boxes[1];
   prm.stages = pl.stages;
   prm.split = pl.split;
   prm.ksteps = pl.ksteps;
@@ -457,7 +504,7 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *A_cat,
     return FLA_ERR_UNSUPPORTED;
   }
   if (pl.split == 1) {
-    bld::build_tc_kernel<<<(unsigned)grid, bld::kThreads, pl.smem_bytes, s>>>(mX, mA, prm);
+    bld::build_tc_kernel<<<(unsigned)grid, bld::kThreads, pl.smem_bytes, s>>>(mX, mW, prm);
     return FLA_OK;
   }
   cudaLaunchConfig_t cfg = {};
@@ -472,7 +519,7 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *A_cat,
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, bld::build_tc_kernel, mX, mA, prm);
+  e = cudaLaunchKernelEx(&cfg, bld::build_tc_kernel, mX, mW, prm);
   if (e != cudaSuccess) {
     build_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;

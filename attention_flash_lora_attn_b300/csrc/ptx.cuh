@@ -286,9 +286,9 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// Cluster-wide barrier over every thread of every CTA of the cluster.  Only
-// used right after set-up, when every CTA of the cluster is resident and
-// reaches it without waiting on anything else.
+// Cluster-wide barrier over every thread of every CTA of the cluster, with
+// release / acquire semantics at cluster scope.  It has no time limit: call it
+// only where every thread of the cluster arrives after bounded waits alone.
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
@@ -307,35 +307,6 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
                : "r"(caddr)
                : "memory");
   return v;
-}
-
-__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// Arrive (release at cluster scope) on an mbarrier of any CTA of the cluster.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
-
-// try_wait with cluster-scope acquire: sees the writes the remote arrivals released.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  }
 }
 
 }  // namespace ptx

@@ -158,10 +158,11 @@ simt_attn_kernel(const SimtAttnParams p) {
 // k-steps of 16 staged in shared memory.  fp32 accumulation.
 // ---------------------------------------------------------------------------
 struct SimtBuildParams {
-  const void *X, *A;  // A: A_cat [D, N] row-major
+  const void *X, *A;  // A: the first of N columns of a row-major weight matrix with row stride lda
   void *L;
   int64_t ldx, ldl, n;
   int32_t D, N;
+  int64_t lda;
 };
 
 template <typename T>
@@ -184,7 +185,7 @@ __global__ void __launch_bounds__(256) simt_build_kernel(const SimtBuildParams p
       // A_cat rows are contiguous along the columns: consecutive threads read consecutive columns
       const int ak = e / 64, ac = e % 64;
       const int gc = col0 + ac, gka = k0 + ak;
-      as[ak][ac] = (gc < p.N && gka < p.D) ? to_f32(Ac[(int64_t)gka * p.N + gc]) : 0.f;
+      as[ak][ac] = (gc < p.N && gka < p.D) ? to_f32(Ac[(int64_t)gka * p.lda + gc]) : 0.f;
     }
     __syncthreads();
 #pragma unroll

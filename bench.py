@@ -568,6 +568,27 @@ def run_legs(args, device, peaks, only=None):
             out["llama8b_decode/non_shared"] = leg
             del ns, Ks, Vs
         del Q, K, V, L, B
+    # ---- ReBaseShared base projection fused with the LR build:
+    #      [K_base | V_base | L] = X . [W_k | W_v | A_cat], one pass over X
+    for leg, wname, rows in (("llama8b_prefill/rebase_kv_lr_build", "llama8b_prefill", None),
+                             ("llama70b_decode/rebase_kv_lr_build", "llama70b_decode", None)):
+        if not want(leg):
+            continue
+        w = WORKLOADS[wname]
+        n = w.build_tokens
+        D, kv, lr = w.d_model, w.hkv * w.head_dim, w.n_agents * w.rank
+        X, W = rnd((n, D)), rnd((D, 2 * kv + lr), D ** -0.5)
+        K = torch.empty((n, w.hkv, w.head_dim), dtype=torch.bfloat16, device=device)
+        V, L = torch.empty_like(K), torch.empty((n, lr), dtype=torch.bfloat16, device=device)
+        t = _median_launch_s(lambda: fla.rebase_kv_lr_build(X, W, hkv=w.hkv, head_dim=w.head_dim,
+                                                            n_agents=w.n_agents, rank=w.rank, K_base=K, V_base=V,
+                                                            L=L), max(3, reps // 2), stream,
+                             flush if n * D * 2 < L2_BYTES else None)
+        flops, byts = 2 * n * D * (2 * kv + lr), (n * D + D * (2 * kv + lr) + n * (2 * kv + lr)) * 2
+        out[leg] = {
+            "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
+            "gbs": byts / t / 1e9, "hbm_frac": byts / t / 1e9 / peaks["hbm_gbs"]}
+        del X, W, K, V, L
     # ---- full LR-cache build, 131072 x 8192 . 8192 x 320
     w = WORKLOADS["llama70b_decode"]
     # the first 16384 rows of the 70B build: a profiler-sized case of the same kernel

@@ -122,6 +122,38 @@ FLA_API fla_status lr_cache_build(const void *X, int64_t ldx, const void *A_cat,
                                   int32_t dtype, int32_t kernel, fla_stream_t stream);
 
 /*
+ * rebase_kv_lr_build - the shared base K/V caches and every agent's LR cache
+ * from one pass over the hidden states:
+ *   [K_base | V_base | L] = X . [W_k | W_v | A_cat]
+ *
+ * PReCache abstract (arxivdaily), ReBaseShared: the shared base cache is
+ * rebuilt from adapter-free hidden states with the pretrained weights;
+ * PreLRShared: each agent's LR cache is computed when the context is
+ * processed.  LRAgent summary, Metodologia section 1: the base value cache
+ * comes from the frozen pretrained projection.  One tensor-core GEMM reads
+ * each tile of X once for all three outputs.  No rotary embedding is applied
+ * to K_base (a caller that uses one applies it afterwards).
+ *
+ *   X        [n_tokens, d_model], row stride ldx elements        (input)
+ *   W_cat    [d_model, 2*hkv*head_dim + n_agents*rank], dense row-major:
+ *            the pretrained key projection W_k [d_model, hkv*head_dim], the
+ *            value projection W_v (same shape) and A_cat = [A_1 | ... | A_A]
+ *            side by side, in that order                         (input)
+ *   K_base   [n_tokens, hkv, head_dim], dense                    (output)
+ *   V_base   [n_tokens, hkv, head_dim], dense                    (output)
+ *   L        [n_tokens, n_agents * rank], row stride ldl         (output)
+ *   dtype, kernel as for lr_cache_build.  The tensor-core path needs bf16,
+ *            d_model % 64 == 0, hkv*head_dim and n_agents*rank multiples of
+ *            32, 16-byte aligned pointers, ldx and ldl multiples of 8.
+ * Errors: FLA_ERR_INVALID_ARG for null pointers with n_tokens > 0, sizes < 1,
+ * ldx < d_model or ldl < n_agents * rank.  n_tokens == 0 is a no-op.
+ */
+FLA_API fla_status rebase_kv_lr_build(const void *X, int64_t ldx, const void *W_cat, void *K_base, void *V_base,
+                                      void *L, int64_t ldl, int64_t n_tokens, int32_t d_model, int32_t hkv,
+                                      int32_t head_dim, int32_t n_agents, int32_t rank, int32_t dtype,
+                                      int32_t kernel, fla_stream_t stream);
+
+/*
  * flash_lora_attn_decode - one query token per agent per request.
  *
  * For request q, agent a, query head j (kv head h = j / (hq/hkv)) and the

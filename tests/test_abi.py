@@ -130,6 +130,27 @@ def test_build_rejects_bad_arguments(lib):
     assert lib.lr_cache_build(p, 64, p, p, 32, 8, 64, 4, 16, 1, 0, None) == 1   # ldl < n_agents * rank
 
 
+def test_rebase_projection_rejects_bad_arguments(lib):
+    p = ctypes.c_void_p(16)
+    ok = (p, 64, p, p, p, p, 16, 8, 64, 1, 64, 1, 16, 1, 0, None)
+
+    def call(**kw):
+        a = list(ok)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return lib.rebase_kv_lr_build(*a)
+    assert call(a7=0) == 0                      # n_tokens == 0: no-op
+    assert call(a1=32) == 1                     # ldx < d_model
+    assert call(a6=8) == 1                      # ldl < n_agents * rank
+    assert call(a0=None) == 1                   # NULL X
+    assert call(a4=None) == 1                   # NULL V_base
+    assert call(a9=0) == 1                      # hkv < 1
+    assert call(a12=0) == 1                     # rank < 1
+    assert call(a13=5) == 1                     # dtype
+    assert call(a14=3) == 2                     # no mma.sync kernel
+    assert call(a13=0, a14=4) == 2              # fp32 is outside the tcgen05 kernel
+
+
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
 def test_valid_call_without_gpu_reports_cuda_error(lib):
     p = ctypes.c_void_p(16)

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import oracle
-from workloads import WORKLOADS, make_build_inputs, make_decode_inputs, make_prefill_inputs
+from workloads import WORKLOADS, make_build_inputs, make_decode_inputs, make_prefill_inputs, make_rebase_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -373,3 +373,64 @@ def test_lr_build_llama70b_full_size_sampled_rows():
     Ls = L[torch.from_numpy(rows).cuda()].double().cpu().numpy()
     ref = oracle.lr_cache_build(x["X"][torch.from_numpy(rows)], x["A_cat"])
     assert _rel_l2(Ls, ref) <= BUILD_RTOL_L2
+
+
+# ----------------------------------------------------------------------------- ReBaseShared base projection
+
+# (n, d_model, hkv, head_dim, n_agents, rank, dtype)
+REBASE = [(1, 64, 1, 64, 2, 16, "bf16"), (77, 256, 2, 64, 3, 32, "bf16"), (300, 512, 8, 128, 4, 16, "bf16"),
+          (1000, 1024, 4, 128, 5, 64, "bf16"), (130, 192, 1, 48, 2, 8, "bf16"), (60, 128, 2, 16, 1, 8, "f32")]
+
+
+def _rebase_check(x, K, V, L, hkv, d):
+    Kr, Vr, Lr = oracle.rebase_kv_lr_build(x["X"], x["W_k"], x["W_v"], x["A_cat"], hkv=hkv, d=d)
+    for got, ref, nm in ((K, Kr, "K_base"), (V, Vr, "V_base"), (L, Lr, "L")):
+        g = got.double().cpu().numpy().reshape(ref.shape)
+        tol = BUILD_RTOL_L2 if got.dtype == torch.bfloat16 else 1e-6
+        assert _rel_l2(g, ref) <= tol, nm
+
+
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
+@pytest.mark.parametrize("case", REBASE, ids=[f"rb{i}" for i in range(len(REBASE))])
+def test_rebase_projection_small(case, kernel):
+    n, D, hkv, d, A, r, dt = case
+    x = make_rebase_inputs(n, D, hkv, d, A, r, torch.bfloat16 if dt == "bf16" else torch.float32, seed=12)
+    W = torch.cat([x["W_k"], x["W_v"], x["A_cat"]], dim=1).cuda()
+    K, V, L = _fla().rebase_kv_lr_build(x["X"].cuda(), W, hkv=hkv, head_dim=d, n_agents=A, rank=r, kernel=kernel)
+    _rebase_check(x, K, V, L, hkv, d)
+
+
+def test_rebase_projection_tensor_kernel_refuses_odd_widths():
+    x = make_rebase_inputs(64, 128, 1, 48, 2, 8, torch.bfloat16, seed=1)
+    W = torch.cat([x["W_k"], x["W_v"], x["A_cat"]], dim=1).cuda()
+    with pytest.raises(_fla().FlaError) as ei:
+        _fla().rebase_kv_lr_build(x["X"].cuda(), W, hkv=1, head_dim=48, n_agents=2, rank=8, kernel="tensor")
+    assert ei.value.status == 2
+
+
+def test_rebase_projection_llama8b_chunk_full():
+    """The 512-token chunk of the 8B workload: X 512x4096 . [W_k | W_v | A_cat] (4096 x 2112), all outputs."""
+    w = WORKLOADS["llama8b_prefill"]
+    x = make_rebase_inputs(w.chunk, w.d_model, w.hkv, w.head_dim, w.n_agents, w.rank, torch.bfloat16, seed=0)
+    W = torch.cat([x["W_k"], x["W_v"], x["A_cat"]], dim=1).cuda()
+    L = torch.full((w.chunk, 104), 7.0, dtype=torch.bfloat16, device="cuda")  # L as a column slice of a wider tensor
+    K, V, Ls = _fla().rebase_kv_lr_build(x["X"].cuda(), W, hkv=w.hkv, head_dim=w.head_dim, n_agents=w.n_agents,
+                                         rank=w.rank, L=L[:, 8:8 + w.n_agents * w.rank], kernel="tensor")
+    _rebase_check(x, K, V, Ls, w.hkv, w.head_dim)
+    Lc = L.double().cpu().numpy()
+    assert (Lc[:, :8] == 7).all() and (Lc[:, 8 + w.n_agents * w.rank:] == 7).all()
+
+
+def test_rebase_projection_llama70b_shape_sampled_rows():
+    """70B shapes (8192 -> 2*1024 + 320 columns) on 16384 rows, 600 sampled rows against the oracle."""
+    w = WORKLOADS["llama70b_decode"]
+    n = 16384
+    x = make_rebase_inputs(n, w.d_model, w.hkv, w.head_dim, w.n_agents, w.rank, torch.bfloat16, seed=3)
+    W = torch.cat([x["W_k"], x["W_v"], x["A_cat"]], dim=1).cuda()
+    K, V, L = _fla().rebase_kv_lr_build(x["X"].cuda(), W, hkv=w.hkv, head_dim=w.head_dim, n_agents=w.n_agents,
+                                        rank=w.rank, kernel="tensor")
+    rows = np.concatenate([[0, 1, 127, 128], np.sort(np.random.default_rng(1).choice(n, 592, replace=False)),
+                           [n - 2, n - 1]])
+    ri = torch.from_numpy(rows)
+    xs = dict(x, X=x["X"][ri])
+    _rebase_check(xs, K[ri.cuda()], V[ri.cuda()], L[ri.cuda()], w.hkv, w.head_dim)

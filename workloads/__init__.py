@@ -168,3 +168,15 @@ def make_build_inputs(n_tokens: int, d_model: int, n_agents: int, rank: int, dty
     X = _randn(gen, (n_tokens, d_model), 1.0, dtype, device)
     A_cat = _randn(gen, (d_model, n_agents * rank), d_model ** -0.5, dtype, device)
     return dict(X=X, A_cat=A_cat)
+
+
+def make_rebase_inputs(n_tokens: int, d_model: int, hkv: int, head_dim: int, n_agents: int, rank: int, dtype,
+                       seed: int = 0, device="cpu") -> Dict[str, torch.Tensor]:
+    """Base-cache rebuild inputs: X [n, D] ~ N(0,1); the pretrained projections
+    W_k, W_v [D, Hkv*d] and A_cat [D, A*r] ~ N(0, 1/D) (unit-variance outputs)."""
+    gen = torch.Generator("cpu").manual_seed(seed)
+    X = _randn(gen, (n_tokens, d_model), 1.0, dtype, device)
+    W_k = _randn(gen, (d_model, hkv * head_dim), d_model ** -0.5, dtype, device)
+    W_v = _randn(gen, (d_model, hkv * head_dim), d_model ** -0.5, dtype, device)
+    A_cat = _randn(gen, (d_model, n_agents * rank), d_model ** -0.5, dtype, device)
+    return dict(X=X, W_k=W_k, W_v=W_v, A_cat=A_cat)
