@@ -680,7 +680,7 @@ inline fla_status decode_t5_launch(const fla_attn_dims &d, float scale, const vo
   mp.r = d.rank;
   mp.part_stride = pl.part_stride; mp.unit_tokens = (int)U; mp.single_len = prm.single_len;
   mp.merge_single = 1;
-  e = launch_merge<dt5::D>(mp, units, grid64, s);
+  e = launch_merge<dt5::D>(mp, decode_units_bound(total_tokens, U), true, s);
   if (e != cudaSuccess) {
     decode_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;

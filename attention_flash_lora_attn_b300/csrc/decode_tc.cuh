@@ -319,6 +319,21 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       for (int b = 0; b < D / 64; ++b)
         ptx::tma_load_2d(dst + (kc * (D / 64) + b) * 2048, &tmB, head * D + b * 64, kc * 16, bar_b);
   };
+  // Q rows of this kv head (zero rows beyond A*G): the global loads are issued
+  // before the stage ring's copies so they are not queued behind them
+  constexpr int kQChunks = C::kRowsPad * (D / 8);
+  constexpr int kQPerThread = (kQChunks + kNT - 1) / kNT;
+  uint4 qv[kQPerThread];
+#pragma unroll
+  for (int i = 0; i < kQPerThread; ++i) {
+    const int e = threadIdx.x + i * kNT;
+    const int row = e / (D / 8), c8 = e % (D / 8);
+    qv[i] = make_uint4(0, 0, 0, 0);
+    if (e < kQChunks && row < p.rows) {
+      const int a = row / p.G, j = head * p.G + row % p.G;
+      qv[i] = *reinterpret_cast<const uint4 *>(p.Q + (((int64_t)q * p.A + a) * p.hq + j) * D + c8 * 8);
+    }
+  }
   int last_issued = -1;  // meaningful in the producer threads only
   if (producer) {
     ptx::prefetch_tmap(&tmK);
@@ -336,15 +351,11 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   const int mt = (warp % C::kGroupWarps) / TG, tg = warp % TG;
   const int g = lane >> 2, t4 = lane & 3;
 
-  // Q rows of this kv head into shared memory (zero rows beyond A*G).
-  for (int e = threadIdx.x; e < C::kRowsPad * (D / 8); e += kNT) {
-    const int row = e / (D / 8), c8 = e % (D / 8);
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (row < p.rows) {
-      const int a = row / p.G, j = head * p.G + row % p.G;
-      v = *reinterpret_cast<const uint4 *>(p.Q + (((int64_t)q * p.A + a) * p.hq + j) * D + c8 * 8);
-    }
-    *reinterpret_cast<uint4 *>(q_smem + row * C::kQPitch + c8 * 16) = v;
+#pragma unroll
+  for (int i = 0; i < kQPerThread; ++i) {
+    const int e = threadIdx.x + i * kNT;
+    if (e < kQChunks)
+      *reinterpret_cast<uint4 *>(q_smem + (e / (D / 8)) * C::kQPitch + (e % (D / 8)) * 16) = qv[i];
   }
   __syncthreads();
   uint32_t qf[D / 16][4];
@@ -720,7 +731,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // decode grid has completed and its writes are visible.  The next decode may
 // start its token loop while this decode's tail and this kernel run.
 // ---------------------------------------------------------------------------
-constexpr int kMergeWarps = 32;   // warps per CTA
 
 struct MergeParams {
   const float *partials;
@@ -731,119 +741,154 @@ struct MergeParams {
   int32_t merge_single;  // 1: single-unit pairs have a partial too (finish them here)
 };
 
-// One warp per query row, no shared memory or barriers: the geometry for
-// merges that fit on the SMs a decode grid leaves idle, or rows with few units.
+// One query row per warp, kMergeLaneWarps warps per CTA, at most 128 registers
+// a thread.  Each warp loads the first RB rows of its B slice into registers
+// before the wait, so once the decode grid ends only the partials' loads (CH
+// units per round) and the combine remain.  A single-request decode leaves
+// enough SMs idle for every merge warp (see decode_unit_tokens), so the whole
+// merge grid is resident early and the next decode can launch behind it.
+constexpr int kMergeLaneWarps = 8;
+
 template <int D>
-__global__ void __launch_bounds__(kMergeWarps * 32) decode_merge_warp_kernel(const MergeParams p) {
+__global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_kernel(const MergeParams p) {
   constexpr int CPL = D / 32;  // accumulator columns per lane
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // The next decode may be scheduled as soon as every CTA of this grid is
-  // resident: its token loop reads only its own inputs and it waits for this
-  // grid before its first global write.  Every grid waited on is then fully
-  // resident (a dependent launches only once all CTAs of its primary have
-  // issued this instruction), so the chain decode -> merge -> decode cannot
-  // deadlock on SM space.
+  constexpr int RB = 16;       // rows of B held in registers from before the wait
+  constexpr int CH = 8;        // units loaded per round
+  const int lane = threadIdx.x & 31;
+  const int gr = blockIdx.x * kMergeLaneWarps + (threadIdx.x >> 5);
+  // the next decode may be scheduled now (see decode_merge_row_kernel)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (gr >= p.n_req * p.hkv * p.rows) return;
+  const int pair = gr / p.rows, row = gr - pair * p.rows;
+  const int q = pair / p.hkv, head = pair - q * p.hkv;
+  const int a = row / p.G, j = head * p.G + row % p.G;
+  // B_a[:, h*d:(h+1)*d] is an input: this lane's columns of its first RB rows
+  const __nv_bfloat16 *bcol = p.B + (int64_t)a * p.r * p.hkv * D + head * D + lane * CPL;
+  const int64_t bstride = (int64_t)p.hkv * D;
+  uint32_t bpre[RB][CPL / 2];
+#pragma unroll
+  for (int i = 0; i < RB; ++i) {
+    if (i < p.r) {
+      if constexpr (CPL == 4) {
+        const uint2 t = __ldg(reinterpret_cast<const uint2 *>(bcol + i * bstride));
+        bpre[i][0] = t.x;
+        bpre[i][1] = t.y;
+      } else {
+        bpre[i][0] = __ldg(reinterpret_cast<const uint32_t *>(bcol + i * bstride));
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < CPL / 2; ++c) bpre[i][c] = 0u;
+    }
+  }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int total = p.n_req * p.hkv * p.rows;
+  int ug0, nu;
+  if (p.single_len >= 0) {
+    ug0 = 0;
+    nu = p.single_len > 0 ? (p.single_len + p.unit_tokens - 1) / p.unit_tokens : 1;
+  } else {
+    const int2 info = __ldcg(p.pair_info + pair);
+    ug0 = info.x;
+    nu = info.y;
+  }
+  if (nu <= 1 && !p.merge_single) return;  // written directly by the decode kernel
   const int W = D + p.r;
   const int64_t ustride = (int64_t)p.hkv * p.part_stride;
-  for (int gr = blockIdx.x * kMergeWarps + warp; gr < total; gr += gridDim.x * kMergeWarps) {
-    const int pair = gr / p.rows, row = gr % p.rows;
-    const int q = pair / p.hkv, head = pair % p.hkv;
-    const int a = row / p.G, j = head * p.G + row % p.G;
-    int ug0, nu;
-    if (p.single_len >= 0) {
-      ug0 = 0;
-      nu = p.single_len > 0 ? (p.single_len + p.unit_tokens - 1) / p.unit_tokens : 1;
-    } else {
-      const int2 info = __ldcg(p.pair_info + pair);
-      ug0 = info.x;
-      nu = info.y;
-    }
-    if (nu <= 1 && !p.merge_single) continue;  // written directly by the decode kernel
-    const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
-    float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
+  const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
+  float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-    constexpr int CH = 4;
-    for (int u0 = 0; u0 < nu; u0 += CH) {
-      float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
+  for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
+  for (int u0 = 0; u0 < nu; u0 += CH) {
+    float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
 #pragma unroll
-      for (int k = 0; k < CH; ++k) {
-        const int u = min(u0 + k, nu - 1);
-        const float *src = base + u * ustride;
-        mu[k] = __ldcg(src + p.rows * W + row);
-        lu[k] = __ldcg(src + p.rows * W + p.rows + row);
-        if constexpr (CPL == 4) {
-          const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * W) + lane);
-          v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
-        } else {
+    for (int k = 0; k < CH; ++k) {
+      const int u = min(u0 + k, nu - 1);
+      const float *src = base + u * ustride;
+      mu[k] = __ldcg(src + p.rows * W + row);
+      lu[k] = __ldcg(src + p.rows * W + p.rows + row);
+      if constexpr (CPL == 4) {
+        const float4 t = __ldcg(reinterpret_cast<const float4 *>(src + row * W) + lane);
+        v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+      } else {
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * W + lane * CPL + c);
-        }
-        a2[k][0] = lane < p.r ? __ldcg(src + row * W + D + lane) : 0.f;
-        a2[k][1] = lane + 32 < p.r ? __ldcg(src + row * W + D + 32 + lane) : 0.f;
+        for (int c = 0; c < CPL; ++c) v[k][c] = __ldcg(src + row * W + lane * CPL + c);
       }
-      float Mc = M;
+      a2[k][0] = lane < p.r ? __ldcg(src + row * W + D + lane) : 0.f;
+      a2[k][1] = lane + 32 < p.r ? __ldcg(src + row * W + D + 32 + lane) : 0.f;
+    }
+    float Mc = M;
 #pragma unroll
-      for (int k = 0; k < CH; ++k)
-        if (u0 + k < nu) Mc = fmaxf(Mc, mu[k]);
-      const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
-      M = Mc;
-      lsum *= sc;
-      pl[0] *= sc;
-      pl[1] *= sc;
+    for (int k = 0; k < CH; ++k)
+      if (u0 + k < nu) Mc = fmaxf(Mc, mu[k]);
+    const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
+    M = Mc;
+    lsum *= sc;
+    pl[0] *= sc;
+    pl[1] *= sc;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) acc[c] *= sc;
+    for (int c = 0; c < CPL; ++c) acc[c] *= sc;
 #pragma unroll
-      for (int k = 0; k < CH; ++k) {
-        if (u0 + k < nu) {
-          const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
-          lsum += w * lu[k];
+    for (int k = 0; k < CH; ++k) {
+      if (u0 + k < nu) {
+        const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
+        lsum += w * lu[k];
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
-          pl[0] += w * a2[k][0];
-          pl[1] += w * a2[k][1];
-        }
+        for (int c = 0; c < CPL; ++c) acc[c] += w * v[k][c];
+        pl[0] += w * a2[k][0];
+        pl[1] += w * a2[k][1];
       }
     }
-    // (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]: lane k holds pl[k] (and pl[k + 32] when r > 32)
-    float lora[CPL];
+  }
+  // (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]: lane k holds pl[k] (and pl[k + 32] when r > 32)
+  float lora[CPL];
 #pragma unroll
-    for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
-    const __nv_bfloat16 *bcol = p.B + (int64_t)a * p.r * p.hkv * D + head * D + lane * CPL;
-    // eight rows of B in flight at a time (each lane reads its CPL columns)
-    constexpr int KB = 8;
-    for (int k0 = 0; k0 < p.r; k0 += KB) {
-      __nv_bfloat16 bv[KB][CPL];
+  for (int c = 0; c < CPL; ++c) lora[c] = 0.f;
 #pragma unroll
-      for (int i = 0; i < KB; ++i) {
-        const int k = min(k0 + i, p.r - 1);
-        const __nv_bfloat16 *bk = bcol + (int64_t)k * p.hkv * D;
-        if constexpr (CPL == 4) {
-          const uint2 t = __ldg(reinterpret_cast<const uint2 *>(bk));
-          bv[i][0] = __ushort_as_bfloat16((unsigned short)(t.x & 0xffffu));
-          bv[i][1] = __ushort_as_bfloat16((unsigned short)(t.x >> 16));
-          bv[i][2] = __ushort_as_bfloat16((unsigned short)(t.y & 0xffffu));
-          bv[i][3] = __ushort_as_bfloat16((unsigned short)(t.y >> 16));
-        } else {
+  for (int i = 0; i < RB; ++i) {
+    const float plk = __shfl_sync(0xffffffffu, pl[0], i);
+    if (i < p.r) {
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) bv[i][c] = bk[c];
-        }
+      for (int c = 0; c < CPL / 2; ++c) {
+        lora[2 * c] += plk * __uint_as_float(bpre[i][c] << 16);
+        lora[2 * c + 1] += plk * __uint_as_float(bpre[i][c] & 0xffff0000u);
       }
+    }
+  }
+  // the remaining rows of B (ranks above RB), eight in flight at a time
+  constexpr int KB = 8;
+  for (int k0 = RB; k0 < p.r; k0 += KB) {
+    uint32_t bv[KB][CPL / 2];
 #pragma unroll
-      for (int i = 0; i < KB; ++i) {
-        const int k = k0 + i;
-        const float plk = __shfl_sync(0xffffffffu, k < 32 ? pl[0] : pl[1], k & 31);
-        if (k < p.r) {
+    for (int i = 0; i < KB; ++i) {
+      const int k = min(k0 + i, p.r - 1);
+      if constexpr (CPL == 4) {
+        const uint2 t = __ldg(reinterpret_cast<const uint2 *>(bcol + k * bstride));
+        bv[i][0] = t.x;
+        bv[i][1] = t.y;
+      } else {
+        bv[i][0] = __ldg(reinterpret_cast<const uint32_t *>(bcol + k * bstride));
+      }
+    }
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) lora[c] += plk * __bfloat162float(bv[i][c]);
+    for (int i = 0; i < KB; ++i) {
+      const int k = k0 + i;
+      const float plk = __shfl_sync(0xffffffffu, k < 32 ? pl[0] : pl[1], k & 31);
+      if (k < p.r) {
+#pragma unroll
+        for (int c = 0; c < CPL / 2; ++c) {
+          lora[2 * c] += plk * __uint_as_float(bv[i][c] << 16);
+          lora[2 * c + 1] += plk * __uint_as_float(bv[i][c] & 0xffff0000u);
         }
       }
     }
-    float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
-    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  }
+  float *out = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D + lane * CPL;
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  if constexpr (CPL == 4) {
+    *reinterpret_cast<float4 *>(out) =
+        make_float4((acc[0] + lora[0]) * inv, (acc[1] + lora[1]) * inv, (acc[2] + lora[2]) * inv,
+                    (acc[3] + lora[3]) * inv);
+  } else {
 #pragma unroll
     for (int c = 0; c < CPL; ++c) out[c] = (acc[c] + lora[c]) * inv;
   }
@@ -870,7 +915,12 @@ __global__ void __launch_bounds__(128) decode_merge_row_kernel(const MergeParams
     reinterpret_cast<uint4 *>(Bs)[e] =
         *reinterpret_cast<const uint4 *>(p.B + ((int64_t)(a * r + k) * p.hkv + head) * D + c8 * 8);
   }
-  // the next decode may be scheduled now (see decode_merge_warp_kernel)
+  // The next decode may be scheduled as soon as every CTA of this grid is
+  // resident: its token loop reads only its own inputs and it waits for this
+  // grid before its first global write.  Every grid waited on is then fully
+  // resident (a dependent launches only once all CTAs of its primary have
+  // issued this instruction), so the chain decode -> merge -> decode cannot
+  // deadlock on SM space.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   int ug0, nu;
@@ -1083,14 +1133,21 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d, bool two_per_sm = false
 
 inline bool decode_tc_shape_supported(const fla_attn_dims &d) { return decode_tc_plan(d).ok; }
 
+// SMs a single-request decode leaves idle for the merge grid behind it: one
+// per 16 merge warps (a warp per query row, at most 128 registers a thread).
+inline int decode_merge_reserve_sms(int hkv, int rows) { return (hkv * rows + 15) / 16; }
+
 // Tokens per work unit.  Single request: split every kv head's context into
-// floor(SMs / hkv) units so one wave covers the GPU.  Several requests: aim at
-// about four units per SM so the block scheduler balances ragged lengths.
-inline int64_t decode_unit_tokens(int n_req, int64_t total_tokens, int hkv) {
+// floor((SMs - merge SMs) / hkv) units, so one wave covers the GPU and the
+// merge's warps find room on the SMs left over (rows = 0: no reservation).
+// Several requests: aim at about four units per SM so the block scheduler
+// balances ragged lengths.
+inline int64_t decode_unit_tokens(int n_req, int64_t total_tokens, int hkv, int rows = 0) {
   const int sms = device_sm_count();
   int64_t U;
   if (n_req == 1) {
-    const int per_head = std::max(1, sms / hkv);
+    const int avail = std::max(hkv, sms - (rows > 0 ? decode_merge_reserve_sms(hkv, rows) : 0));
+    const int per_head = std::max(1, avail / hkv);
     U = (total_tokens + per_head - 1) / per_head;
   } else {
     const int64_t target_units = (int64_t)sms * 4;
@@ -1099,7 +1156,7 @@ inline int64_t decode_unit_tokens(int n_req, int64_t total_tokens, int hkv) {
   // at most kMaxUnitsPerPair units per (request, head)
   U = std::max<int64_t>(U, (total_tokens + dec::kMaxUnitsPerPair - 1) / dec::kMaxUnitsPerPair);
   U = std::max<int64_t>(U, 32);
-  U = (U + 15) / 16 * 16;
+  U = (U + 63) / 64 * 64;  // whole 64-token tiles: no unit ends on a nearly empty tile
   return U;
 }
 
@@ -1110,7 +1167,7 @@ inline int64_t decode_max_units(int n_req, int64_t total_tokens, int64_t U) {
 inline size_t decode_tc_workspace_bytes(const fla_attn_dims &d, int n_req, int64_t total_tokens) {
   const DecodePlan pl = decode_tc_plan(d);
   if (!pl.ok || n_req <= 0) return 0;
-  const int64_t U = decode_unit_tokens(n_req, std::max<int64_t>(total_tokens, 1), d.hkv);
+  const int64_t U = decode_unit_tokens(n_req, std::max<int64_t>(total_tokens, 1), d.hkv, pl.rows);
   const int64_t units = decode_max_units(n_req, total_tokens, U);
   const size_t info = ((size_t)n_req * d.hkv * sizeof(int2) + 255) / 256 * 256;
   const size_t part = (size_t)units * d.hkv * pl.part_stride * 4;
@@ -1140,40 +1197,30 @@ inline CUtensorMapSwizzle swizzle_enum(int bytes) {
                       : bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
 }
 
-// Merge-kernel geometry.  One warp per row keeps the CTA count small: when
-// those CTAs fit on the SMs the decode grid leaves idle, they are resident
-// before the decode ends and the next decode's CTAs take every SM the decode
-// frees.  Rows with many units are merged faster by four warps each.
-struct MergeShape {
-  int wpr;
-  unsigned grid;
-};
-inline MergeShape merge_shape(int n_req, int hkv, int rows, int64_t units_total, int64_t decode_grid) {
-  const int64_t total = (int64_t)n_req * hkv * rows;
-  const int64_t one = (total + dec::kMergeWarps - 1) / dec::kMergeWarps;
-  const int64_t idle = std::max<int64_t>(0, device_sm_count() - decode_grid);
-  const bool few_units = units_total <= 4 * (int64_t)n_req;
-  if (one <= idle || few_units) return MergeShape{1, (unsigned)std::max<int64_t>(1, one)};
-  return MergeShape{4, (unsigned)total};
-}
+// Merge-kernel geometry: one warp per query row (kMergeLaneWarps rows per CTA),
+// or, for rows with many units (or when the caller asks for it), four warps
+// per row in one CTA each.
+constexpr int kLaneMaxUnits = 32;
 
 // Launches the merge kernel behind a decode kernel (programmatic dependent launch).
+// nu_bound: an upper bound on the units of any (request, head) pair.
 template <int D>
-inline cudaError_t launch_merge(const dec::MergeParams &mp, int64_t units_total, int64_t decode_grid, cudaStream_t s) {
-  const MergeShape ms = merge_shape(mp.n_req, mp.hkv, mp.rows, units_total, decode_grid);
+inline cudaError_t launch_merge(const dec::MergeParams &mp, int64_t nu_bound, bool prefer_rows, cudaStream_t s) {
+  const int64_t total = (int64_t)mp.n_req * mp.hkv * mp.rows;
+  const bool lane = !prefer_rows && nu_bound <= kLaneMaxUnits;
   cudaLaunchConfig_t cfg = {};
-  // one-warp kernel: a 1-D grid of 32-row CTAs; four-warp kernel: (pair, row)
-  cfg.gridDim = ms.wpr == 1 ? dim3(ms.grid) : dim3((unsigned)(mp.n_req * mp.hkv), (unsigned)mp.rows);
-  cfg.blockDim = dim3(ms.wpr == 1 ? dec::kMergeWarps * 32 : 4 * 32);
+  cfg.gridDim = lane ? dim3((unsigned)((total + dec::kMergeLaneWarps - 1) / dec::kMergeLaneWarps))
+                     : dim3((unsigned)(mp.n_req * mp.hkv), (unsigned)mp.rows);
+  cfg.blockDim = dim3(lane ? dec::kMergeLaneWarps * 32 : 4 * 32);
   // the four-warp kernel: this row's B slice plus the cross-warp combine buffer
-  cfg.dynamicSmemBytes = ms.wpr == 1 ? 0 : (size_t)mp.r * D * 2 + 4 * 32 * (D / 32 + 4) * 4;
+  cfg.dynamicSmemBytes = lane ? 0 : (size_t)mp.r * D * 2 + 4 * 32 * (D / 32 + 4) * 4;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  if (ms.wpr == 1) return cudaLaunchKernelEx(&cfg, dec::decode_merge_warp_kernel<D>, mp);
+  if (lane) return cudaLaunchKernelEx(&cfg, dec::decode_merge_lane_kernel<D>, mp);
   if (cfg.dynamicSmemBytes > 48 * 1024) {
     const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(dec::decode_merge_row_kernel<D>),
                                               (int)cfg.dynamicSmemBytes);
@@ -1182,10 +1229,15 @@ inline cudaError_t launch_merge(const dec::MergeParams &mp, int64_t units_total,
   return cudaLaunchKernelEx(&cfg, dec::decode_merge_row_kernel<D>, mp);
 }
 
+// Upper bound on the units of one (request, head) pair.
+inline int64_t decode_units_bound(int64_t total_tokens, int64_t U) {
+  return std::max<int64_t>(1, std::min<int64_t>(dec::kMaxUnitsPerPair, (total_tokens + U - 1) / U));
+}
+
 template <int D, int MT, int TG, int NLT, int SG>
 inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, const CUtensorMap &mV,
                                 const CUtensorMap &mL, const CUtensorMap &mB, const dec::Params &prm, unsigned grid,
-                                bool need_merge, cudaStream_t s) {
+                                bool need_merge, int64_t nu_bound, cudaStream_t s) {
   auto kern = dec::decode_tc_kernel<D, MT, TG, NLT, SG>;
   cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), pl.smem_bytes);
   if (e != cudaSuccess) {
@@ -1218,7 +1270,7 @@ inline fla_status decode_tc_run(const DecodePlan &pl, const CUtensorMap &mK, con
   mp.n_req = prm.n_req; mp.A = prm.A; mp.hq = prm.hq; mp.hkv = prm.hkv; mp.G = prm.G; mp.rows = prm.rows;
   mp.r = prm.r;
   mp.part_stride = prm.part_stride; mp.unit_tokens = prm.unit_tokens; mp.single_len = prm.single_len;
-  e = launch_merge<D>(mp, grid / prm.hkv, grid, s);
+  e = launch_merge<D>(mp, nu_bound, false, s);
   if (e != cudaSuccess) {
     decode_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;
@@ -1240,7 +1292,7 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
     decode_tc_err() = "cuTensorMapEncodeTiled is not available from the driver";
     return FLA_ERR_CUDA;
   }
-  const int64_t U = decode_unit_tokens(n_req, total_tokens, d.hkv);
+  const int64_t U = decode_unit_tokens(n_req, total_tokens, d.hkv, pl.rows);
   const int64_t units = decode_max_units(n_req, total_tokens, U);
   if (units * d.hkv > 2 * (int64_t)device_sm_count()) {
     // several waves of CTAs: two per SM where the shape allows
@@ -1316,7 +1368,8 @@ inline fla_status decode_tc_launch(const fla_attn_dims &d, float scale, const vo
   const bool need_merge = !(n_req == 1 && total_tokens <= U);
 #define FLA_DEC_CASE(DD, MM, TT, NN, GG)                                                    \
   if (pl.D == DD && pl.MT == MM && pl.TG == TT && pl.NLT == NN && pl.SG == GG)              \
-    return decode_tc_run<DD, MM, TT, NN, GG>(pl, mK, mV, mL, mB, prm, grid, need_merge, s);
+    return decode_tc_run<DD, MM, TT, NN, GG>(pl, mK, mV, mL, mB, prm, grid, need_merge,          \
+                                             decode_units_bound(total_tokens, U), s);
   FLA_DEC_CASE(128, 1, 4, 8, 2) FLA_DEC_CASE(128, 1, 4, 16, 2)
   FLA_DEC_CASE(128, 1, 4, 8, 1) FLA_DEC_CASE(128, 1, 4, 16, 1)
   FLA_DEC_CASE(128, 2, 4, 8, 1) FLA_DEC_CASE(128, 2, 4, 16, 1)
