@@ -253,6 +253,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   // bars: full[stages] | empty[stages] | B loaded | merge batch
   __shared__ int s_info[8];   // q, unit, n_units, token begin, token count, found
   __shared__ int s_flag[1];   // abort
+  __shared__ int s_last_issue[8];  // last tile copied into each stage (drained on an abort)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int head = blockIdx.x % p.hkv;
@@ -270,6 +271,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) {
       s_info[5] = found;
       s_flag[0] = 0;
+      for (int s = 0; s < 8; ++s) s_last_issue[s] = -1;
       for (int s = 0; s < p.stages; ++s) {
         ptx::mbar_init(ptx::smem_u32(&bars[s]), 1);                   // full: one arrive + tx bytes
         ptx::mbar_init(ptx::smem_u32(&bars[p.stages + s]), C::kGroupWarps);  // empty: one arrive per warp of the group
@@ -298,6 +300,7 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 
   auto issue_tile = [&](int it) {
     const int st = it % p.stages;
+    s_last_issue[st] = it;
     const uint32_t fb = bar_full0 + 8 * st;
     ptx::mbar_arrive_expect_tx(fb, stage_bytes);
     const uint32_t sbase = ptx::smem_u32(smem + st * stage_bytes);
@@ -334,14 +337,12 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       qv[i] = *reinterpret_cast<const uint4 *>(p.Q + (((int64_t)q * p.A + a) * p.hq + j) * D + c8 * 8);
     }
   }
-  int last_issued = -1;  // meaningful in the producer threads only
   if (producer) {
     ptx::prefetch_tmap(&tmK);
     ptx::prefetch_tmap(&tmV);
     ptx::prefetch_tmap(&tmL);
     for (int it = grp; it < p.stages && it < n_tiles; it += SG) {
       issue_tile(it);
-      last_issued = it;
     }
     // B is applied here only when this CTA is the only unit of its (q, head);
     // otherwise the merge kernel applies it once after combining the units
@@ -500,7 +501,8 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     __syncwarp();
     if (lane == 0) ptx::mbar_arrive(bar_empty0 + 8 * st);
     // ---- refill: once every warp of the group has released this stage, load
-    //      tile it + stages (the same group's, as stages % SG == 0)
+    //      tile it + stages into it (with an odd stage count that tile belongs
+    //      to the other group, whose warps wait on this stage's full barrier)
     if (producer && it + p.stages < n_tiles) {
       if (!ptx::mbar_wait(bar_empty0 + 8 * st, (it / p.stages) & 1)) {
         set_device_error(kErrDecodeEmptyWait);
@@ -508,7 +510,6 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         break;
       }
       issue_tile(it + p.stages);
-      last_issued = it + p.stages;
     }
   }
   if (aborted) s_flag[0] = 1;
@@ -523,24 +524,36 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
   if (s_flag[0]) {
     // Do not leave while copies are in flight: wait (bounded) for the last
     // load issued into each stage.
-    if (producer) {
-      for (int it = last_issued; it >= 0 && it > last_issued - p.stages; it -= SG)
-        ptx::mbar_wait(bar_full0 + 8 * (it % p.stages), (it / p.stages) & 1);
-      if (p.bs_dedicated && grp == 0 && n_units == 1) ptx::mbar_wait(bar_b, 0);
+    if (threadIdx.x == 0) {
+      for (int st = 0; st < p.stages; ++st) {
+        const int it = s_last_issue[st];
+        if (it >= 0) ptx::mbar_wait(bar_full0 + 8 * st, (it / p.stages) & 1);
+      }
     }
+    if (producer && p.bs_dedicated && grp == 0 && n_units == 1) ptx::mbar_wait(bar_b, 0);
     return;
   }
   // Every issued tile was waited on by every warp, so no TMA write is pending:
   // the stage ring is reused below.
 
-  const bool single = (n_units == 1);
-
   // ---- merge the SG*TG token slices of each row tile in one pass: every warp
   //      publishes its fragments into the free ring (one float4 per n-tile and
   //      lane, thread-linear, conflict-free); after one barrier each warp
   //      combines a strided share of the n-tiles over all slices of its row
-  //      tile and writes the result into the slot of the tile's slice 0.  The
-  //      tile's running max and row sum go to a small table after the slots.
+  //      tile.  A CTA that is one of several units of its (q, head) stores the
+  //      result straight into its partial record ([rows][D + r] (P.V_base |
+  //      own agent's P.L_a) | m[rows] | l[rows]); the only unit of a context
+  //      writes it into the slot of the tile's slice 0 (and the tile's running
+  //      max and row sum into a small table) for the B epilogue below.
+  const bool single = (n_units == 1);
+  const int W = D + p.r;
+  float *part = p.partials + ((int64_t)slot * p.hkv + head) * p.part_stride;
+  if (!single) {
+    // the first global write: the previous grid of the stream (this library's
+    // merge, which reads the workspace) must have finished
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(slot - unit, n_units);
+  }
   constexpr int NS = C::kSlices;
   constexpr int NQ = D / 8 + NLT;  // float4 groups per lane: acc_v n-tiles | acc_l n-tiles
   constexpr int NV4 = NQ + 1;      // + (m0, m1, l0, l1)
@@ -575,6 +588,9 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
       f0[k] = (f0[k] == -INFINITY) ? 0.f : ptx::ex2(f0[k] - M0);
       f1[k] = (f1[k] == -INFINITY) ? 0.f : ptx::ex2(f1[k] - M1);
     }
+    const int r0 = row_lo + g, r1 = row_lo + g + 8;  // this lane's rows (x, y: r0; z, w: r1)
+    // own agent's first column within the tile's L window, per row
+    const int blk0 = (r0 / p.G - a_lo) * p.l_agent_stride, blk1 = (r1 / p.G - a_lo) * p.l_agent_stride;
 #pragma unroll
     for (int jj = 0; jj < NQ / NS; ++jj) {
       const int i = jj * NS + kslice;  // fragment elements x, y: row g; z, w: row g + 8
@@ -587,7 +603,19 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         acc.z = fmaf(f1[k], v.z, acc.z);
         acc.w = fmaf(f1[k], v.w, acc.w);
       }
-      xch[(slice_warp(0) * NV4 + i) * 32 + lane] = acc;  // n-tile i is read and written by this warp alone
+      if (single) {
+        xch[(slice_warp(0) * NV4 + i) * 32 + lane] = acc;  // n-tile i is read and written by this warp alone
+      } else if (i < D / 8) {
+        const int col = i * 8 + 2 * t4;
+        if (r0 < p.rows) *reinterpret_cast<float2 *>(part + r0 * W + col) = make_float2(acc.x, acc.y);
+        if (r1 < p.rows) *reinterpret_cast<float2 *>(part + r1 * W + col) = make_float2(acc.z, acc.w);
+      } else {
+        const int cc = (i - D / 8) * 8 + 2 * t4;  // window column (cc, cc + 1 share an agent: r is even)
+        if (r0 < p.rows && cc >= blk0 && cc < blk0 + p.r)
+          *reinterpret_cast<float2 *>(part + r0 * W + D + cc - blk0) = make_float2(acc.x, acc.y);
+        if (r1 < p.rows && cc >= blk1 && cc < blk1 + p.r)
+          *reinterpret_cast<float2 *>(part + r1 * W + D + cc - blk1) = make_float2(acc.z, acc.w);
+      }
     }
     if (kslice == 0) {
       float L0 = 0.f, L1 = 0.f;
@@ -597,122 +625,103 @@ decode_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         L0 = fmaf(f0[k], ml.z, L0);
         L1 = fmaf(f1[k], ml.w, L1);
       }
-      mlx[mt * 32 + lane] = make_float4(M0, M1, L0, L1);
-    }
-  }
-  __syncthreads();
-
-  const int row0 = row_lo + g, row1 = row_lo + g + 8;
-  if (single) {
-    if (kslice == 0) {
-      const float4 *src = xch + warp * NV4 * 32 + lane;
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        const float4 v = src[i * 32];
-        acc_v[i][0] = v.x; acc_v[i][1] = v.y; acc_v[i][2] = v.z; acc_v[i][3] = v.w;
-      }
-#pragma unroll
-      for (int i = 0; i < NLT; ++i) {
-        const float4 v = src[(D / 8 + i) * 32];
-        acc_l[i][0] = v.x; acc_l[i][1] = v.y; acc_l[i][2] = v.z; acc_l[i][3] = v.w;
-      }
-      const float4 ml = mlx[mt * 32 + lane];
-      l0 = ml.z;
-      l1 = ml.w;
-    }
-    if (!p.bs_dedicated) {
-      // the B slices are staged in the ring the fragments were just read from
-      ptx::fence_proxy_async_smem();
-      __syncthreads();
-    }
-    // ---- B slices: prefetched at the start, or loaded now into the free ring
-    uint8_t *bs = p.bs_dedicated ? bsm : smem;
-    if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
-    if (!ptx::mbar_wait(bar_b, 0)) {
-      set_device_error(kErrDecodeFullWait);
-      return;  // the only copy in flight is the one that never completed
-    }
-    if (kslice != 0) return;
-    // ---- acc_v += (P.L_a) . B_a for this warp's rows (K = window columns of agent a)
-    {
-      const int ag0 = row0 < p.rows ? row0 / p.G : -1;
-      const int ag1 = row1 < p.rows ? row1 / p.G : -1;
-#pragma unroll
-      for (int ks = 0; ks < NLT / 2; ++ks) {
-        if (ks * 16 >= win) break;  // warp-uniform
-        for (int a = a_lo; a <= a_hi; ++a) {
-          const int blk = a * p.l_agent_stride - c_lo;          // agent a's first window column
-          if (ks * 16 < blk || ks * 16 >= blk + p.r) continue;  // this k-step is not agent a's
-          const int kb = ks * 16 - blk;                          // first row of B_a for this k-step
-          const bool own0 = (ag0 == a), own1 = (ag1 == a);
-          uint32_t ah[4], al[4];
-          ah[0] = pack_hi_lo(own0 ? acc_l[2 * ks][0] : 0.f, own0 ? acc_l[2 * ks][1] : 0.f, al[0]);
-          ah[1] = pack_hi_lo(own1 ? acc_l[2 * ks][2] : 0.f, own1 ? acc_l[2 * ks][3] : 0.f, al[1]);
-          ah[2] = pack_hi_lo(own0 ? acc_l[2 * ks + 1][0] : 0.f, own0 ? acc_l[2 * ks + 1][1] : 0.f, al[2]);
-          ah[3] = pack_hi_lo(own1 ? acc_l[2 * ks + 1][2] : 0.f, own1 ? acc_l[2 * ks + 1][3] : 0.f, al[3]);
-          const int mi = lane >> 3, ri = lane & 7;
-          const int rr = (mi & 1) * 8 + ri;                 // row within the 16-row box
-          const int kc = (a * p.r + kb) >> 4;               // 16-row box index
-          const uint32_t bbox = ptx::smem_u32(bs) + kc * (D / 64) * 2048 + rr * 128;
-#pragma unroll
-          for (int dp = 0; dp < D / 16; ++dp) {
-            const int c16 = dp * 2 + (mi >> 1);
-            uint32_t bb[4];
-            ptx::ldsm_x4_t(bbox + (c16 >> 3) * 2048 + (swz_chunk(c16 & 7, rr, 128) << 4), bb);
-            ptx::mma_bf16(acc_v[2 * dp], ah, bb[0], bb[1]);
-            ptx::mma_bf16(acc_v[2 * dp + 1], ah, bb[2], bb[3]);
-            ptx::mma_bf16(acc_v[2 * dp], al, bb[0], bb[1]);
-            ptx::mma_bf16(acc_v[2 * dp + 1], al, bb[2], bb[3]);
-          }
+      if (single) {
+        mlx[mt * 32 + lane] = make_float4(M0, M1, L0, L1);
+      } else if (t4 == 0) {
+        if (r0 < p.rows) {
+          part[p.rows * W + r0] = M0;
+          part[p.rows * W + p.rows + r0] = L0;
+        }
+        if (r1 < p.rows) {
+          part[p.rows * W + r1] = M1;
+          part[p.rows * W + p.rows + r1] = L1;
         }
       }
     }
-    // ---- O = (P.V_base + (P.L_a).B_a) / l, straight from the fragments
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(slot - unit, n_units);
-    const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-#pragma unroll
-    for (int h2 = 0; h2 < 2; ++h2) {
-      const int row = h2 ? row1 : row0;
-      if (row >= p.rows) continue;
-      const int a = row / p.G, j = head * p.G + row % p.G;
-      float *o = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D;
-      const float inv = h2 ? inv1 : inv0;
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i)
-        *reinterpret_cast<float2 *>(o + i * 8 + 2 * t4) =
-            make_float2(acc_v[i][2 * h2] * inv, acc_v[i][2 * h2 + 1] * inv);
-    }
-    return;
   }
+  if (!single) return;  // the partial record is complete
+  __syncthreads();
 
-  // ---- several units: publish this unit's partial from the merged slots in
-  //      record order, a row per warp and consecutive columns per lane:
-  //      [rows][D + r] (P.V_base | own agent's P.L_a) | m[rows] | l[rows]
+  // ---- the only unit of its context: (P.L_a).B_a and O, in this CTA
+  const int row0 = row_lo + g, row1 = row_lo + g + 8;
+  if (kslice == 0) {
+    const float4 *src = xch + warp * NV4 * 32 + lane;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      const float4 v = src[i * 32];
+      acc_v[i][0] = v.x; acc_v[i][1] = v.y; acc_v[i][2] = v.z; acc_v[i][3] = v.w;
+    }
+#pragma unroll
+    for (int i = 0; i < NLT; ++i) {
+      const float4 v = src[(D / 8 + i) * 32];
+      acc_l[i][0] = v.x; acc_l[i][1] = v.y; acc_l[i][2] = v.z; acc_l[i][3] = v.w;
+    }
+    const float4 ml = mlx[mt * 32 + lane];
+    l0 = ml.z;
+    l1 = ml.w;
+  }
+  if (!p.bs_dedicated) {
+    // the B slices are staged in the ring the fragments were just read from
+    ptx::fence_proxy_async_smem();
+    __syncthreads();
+  }
+  // ---- B slices: prefetched at the start, or loaded now into the free ring
+  uint8_t *bs = p.bs_dedicated ? bsm : smem;
+  if (!p.bs_dedicated && threadIdx.x == 0) issue_B(ptx::smem_u32(bs));
+  if (!ptx::mbar_wait(bar_b, 0)) {
+    set_device_error(kErrDecodeFullWait);
+    return;  // the only copy in flight is the one that never completed
+  }
+  if (kslice != 0) return;
+  // ---- acc_v += (P.L_a) . B_a for this warp's rows (K = window columns of agent a)
+  {
+    const int ag0 = row0 < p.rows ? row0 / p.G : -1;
+    const int ag1 = row1 < p.rows ? row1 / p.G : -1;
+#pragma unroll
+    for (int ks = 0; ks < NLT / 2; ++ks) {
+      if (ks * 16 >= win) break;  // warp-uniform
+      for (int a = a_lo; a <= a_hi; ++a) {
+        const int blk = a * p.l_agent_stride - c_lo;          // agent a's first window column
+        if (ks * 16 < blk || ks * 16 >= blk + p.r) continue;  // this k-step is not agent a's
+        const int kb = ks * 16 - blk;                          // first row of B_a for this k-step
+        const bool own0 = (ag0 == a), own1 = (ag1 == a);
+        uint32_t ah[4], al[4];
+        ah[0] = pack_hi_lo(own0 ? acc_l[2 * ks][0] : 0.f, own0 ? acc_l[2 * ks][1] : 0.f, al[0]);
+        ah[1] = pack_hi_lo(own1 ? acc_l[2 * ks][2] : 0.f, own1 ? acc_l[2 * ks][3] : 0.f, al[1]);
+        ah[2] = pack_hi_lo(own0 ? acc_l[2 * ks + 1][0] : 0.f, own0 ? acc_l[2 * ks + 1][1] : 0.f, al[2]);
+        ah[3] = pack_hi_lo(own1 ? acc_l[2 * ks + 1][2] : 0.f, own1 ? acc_l[2 * ks + 1][3] : 0.f, al[3]);
+        const int mi = lane >> 3, ri = lane & 7;
+        const int rr = (mi & 1) * 8 + ri;                 // row within the 16-row box
+        const int kc = (a * p.r + kb) >> 4;               // 16-row box index
+        const uint32_t bbox = ptx::smem_u32(bs) + kc * (D / 64) * 2048 + rr * 128;
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          const int c16 = dp * 2 + (mi >> 1);
+          uint32_t bb[4];
+          ptx::ldsm_x4_t(bbox + (c16 >> 3) * 2048 + (swz_chunk(c16 & 7, rr, 128) << 4), bb);
+          ptx::mma_bf16(acc_v[2 * dp], ah, bb[0], bb[1]);
+          ptx::mma_bf16(acc_v[2 * dp + 1], ah, bb[2], bb[3]);
+          ptx::mma_bf16(acc_v[2 * dp], al, bb[0], bb[1]);
+          ptx::mma_bf16(acc_v[2 * dp + 1], al, bb[2], bb[3]);
+        }
+      }
+    }
+  }
+  // ---- O = (P.V_base + (P.L_a).B_a) / l, straight from the fragments
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (unit == 0 && threadIdx.x == 0) p.pair_info[q * p.hkv + head] = make_int2(slot - unit, n_units);
-  {
-    const int W = D + p.r;
-    float *dst = p.partials + ((int64_t)slot * p.hkv + head) * p.part_stride;
-    const float *xf = reinterpret_cast<const float *>(xch);
-    for (int row = warp; row < p.rows; row += C::kWarps) {
-      const int tile = row >> 4, hi = (row >> 3) & 1, gg = row & 7;
-      // slot of the tile's slice 0 (warp tile * TG of group 0), as floats
-      const float *src = xf + tile * TG * NV4 * 32 * 4;
-      // own agent's first column within the tile's L window
-      const int blk = (row / p.G - (tile * 16) / p.G) * p.l_agent_stride;
-      float *drow = dst + row * W;
-      for (int col = lane; col < W; col += 32) {
-        const int cc = col < D ? col : blk + col - D;
-        const int i = col < D ? (cc >> 3) : D / 8 + (cc >> 3);
-        drow[col] = src[(i * 32 + gg * 4 + ((cc & 7) >> 1)) * 4 + hi * 2 + (cc & 1)];
-      }
-      if (lane == 0) {
-        const float4 ml = mlx[tile * 32 + gg * 4];
-        dst[p.rows * W + row] = hi ? ml.y : ml.x;
-        dst[p.rows * W + p.rows + row] = hi ? ml.w : ml.z;
-      }
-    }
+  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+#pragma unroll
+  for (int h2 = 0; h2 < 2; ++h2) {
+    const int row = h2 ? row1 : row0;
+    if (row >= p.rows) continue;
+    const int a = row / p.G, j = head * p.G + row % p.G;
+    float *o = p.O + (((int64_t)q * p.A + a) * p.hq + j) * D;
+    const float inv = h2 ? inv1 : inv0;
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<float2 *>(o + i * 8 + 2 * t4) =
+          make_float2(acc_v[i][2 * h2] * inv, acc_v[i][2 * h2 + 1] * inv);
   }
 }
 
@@ -741,24 +750,30 @@ struct MergeParams {
   int32_t merge_single;  // 1: single-unit pairs have a partial too (finish them here)
 };
 
-// One query row per warp, kMergeLaneWarps warps per CTA, at most 128 registers
-// a thread.  Each warp loads the first RB rows of its B slice into registers
-// before the wait, so once the decode grid ends only the partials' loads (CH
-// units per round) and the combine remain.  A single-request decode leaves
-// enough SMs idle for every merge warp (see decode_unit_tokens), so the whole
-// merge grid is resident early and the next decode can launch behind it.
+// Two warps per query row (kMergeLaneWarps / 2 rows per CTA), at most 128
+// registers a thread.  Each warp combines half of the row's units, CH units
+// per round of loads; the second half is folded into the first through shared
+// memory (first half first: a fixed order).  The first warp of a row loads the
+// first RB rows of its B slice into registers before the wait, so once the
+// decode grid ends only the partials' loads and the combine remain.  A
+// single-request decode leaves enough SMs idle for every merge warp (see
+// decode_unit_tokens), so the whole merge grid is resident early and the next
+// decode can launch behind it.
 constexpr int kMergeLaneWarps = 8;
+static_assert(kMergeLaneWarps / 2 <= 4, "one named barrier (ids 1..4) per row of a CTA");
 
 template <int D>
 __global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_kernel(const MergeParams p) {
   constexpr int CPL = D / 32;  // accumulator columns per lane
   constexpr int RB = 16;       // rows of B held in registers from before the wait
   constexpr int CH = 8;        // units loaded per round
-  const int lane = threadIdx.x & 31;
-  const int gr = blockIdx.x * kMergeLaneWarps + (threadIdx.x >> 5);
+  __shared__ float xw[kMergeLaneWarps / 2][CPL + 4][32];  // the second warp's state, per row
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rl = warp >> 1, half = warp & 1;
+  const int gr = blockIdx.x * (kMergeLaneWarps / 2) + rl;
   // the next decode may be scheduled now (see decode_merge_row_kernel)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (gr >= p.n_req * p.hkv * p.rows) return;
+  if (gr >= p.n_req * p.hkv * p.rows) return;  // both warps of the row
   const int pair = gr / p.rows, row = gr - pair * p.rows;
   const int q = pair / p.hkv, head = pair - q * p.hkv;
   const int a = row / p.G, j = head * p.G + row % p.G;
@@ -768,7 +783,7 @@ __global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_ker
   uint32_t bpre[RB][CPL / 2];
 #pragma unroll
   for (int i = 0; i < RB; ++i) {
-    if (i < p.r) {
+    if (half == 0 && i < p.r) {
       if constexpr (CPL == 4) {
         const uint2 t = __ldg(reinterpret_cast<const uint2 *>(bcol + i * bstride));
         bpre[i][0] = t.x;
@@ -791,18 +806,20 @@ __global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_ker
     ug0 = info.x;
     nu = info.y;
   }
-  if (nu <= 1 && !p.merge_single) return;  // written directly by the decode kernel
+  if (nu <= 1 && !p.merge_single) return;  // written directly by the decode kernel (both warps)
   const int W = D + p.r;
   const int64_t ustride = (int64_t)p.hkv * p.part_stride;
   const float *base = p.partials + ((int64_t)ug0 * p.hkv + head) * p.part_stride;
+  const int nh = (nu + 1) / 2;
+  const int ub = half ? nh : 0, ue = half ? nu : nh;  // this warp's units
   float M = -INFINITY, lsum = 0.f, acc[CPL], pl[2] = {0.f, 0.f};
 #pragma unroll
   for (int c = 0; c < CPL; ++c) acc[c] = 0.f;
-  for (int u0 = 0; u0 < nu; u0 += CH) {
+  for (int u0 = ub; u0 < ue; u0 += CH) {
     float mu[CH], lu[CH], v[CH][CPL], a2[CH][2];
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-      const int u = min(u0 + k, nu - 1);
+      const int u = min(u0 + k, ue - 1);
       const float *src = base + u * ustride;
       mu[k] = __ldcg(src + p.rows * W + row);
       lu[k] = __ldcg(src + p.rows * W + p.rows + row);
@@ -819,7 +836,7 @@ __global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_ker
     float Mc = M;
 #pragma unroll
     for (int k = 0; k < CH; ++k)
-      if (u0 + k < nu) Mc = fmaxf(Mc, mu[k]);
+      if (u0 + k < ue) Mc = fmaxf(Mc, mu[k]);
     const float sc = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mc);
     M = Mc;
     lsum *= sc;
@@ -829,7 +846,7 @@ __global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_ker
     for (int c = 0; c < CPL; ++c) acc[c] *= sc;
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
-      if (u0 + k < nu) {
+      if (u0 + k < ue) {
         const float w = (mu[k] == -INFINITY) ? 0.f : ptx::ex2(mu[k] - M);
         lsum += w * lu[k];
 #pragma unroll
@@ -838,6 +855,34 @@ __global__ void __launch_bounds__(kMergeLaneWarps * 32, 2) decode_merge_lane_ker
         pl[1] += w * a2[k][1];
       }
     }
+  }
+  // fold the second half into the first
+  if (half) {
+    xw[rl][0][lane] = M;
+    xw[rl][1][lane] = lsum;
+    xw[rl][2][lane] = pl[0];
+    xw[rl][3][lane] = pl[1];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) xw[rl][4 + c][lane] = acc[c];
+  }
+  // the row's two warps (constant barrier ids keep the CTA's barrier count low)
+  switch (rl) {
+    case 0: asm volatile("bar.sync 1, 64;" ::: "memory"); break;
+    case 1: asm volatile("bar.sync 2, 64;" ::: "memory"); break;
+    case 2: asm volatile("bar.sync 3, 64;" ::: "memory"); break;
+    default: asm volatile("bar.sync 4, 64;" ::: "memory"); break;
+  }
+  if (half) return;
+  {
+    const float M1 = xw[rl][0][lane];
+    const float Mt = fmaxf(M, M1);
+    const float w0 = (M == -INFINITY) ? 0.f : ptx::ex2(M - Mt);
+    const float w1 = (M1 == -INFINITY) ? 0.f : ptx::ex2(M1 - Mt);
+    lsum = w0 * lsum + w1 * xw[rl][1][lane];
+    pl[0] = w0 * pl[0] + w1 * xw[rl][2][lane];
+    pl[1] = w0 * pl[1] + w1 * xw[rl][3][lane];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[c] = w0 * acc[c] + w1 * xw[rl][4 + c][lane];
   }
   // (sum_u w_u pl_u) . B_a[:, h*d:(h+1)*d]: lane k holds pl[k] (and pl[k + 32] when r > 32)
   float lora[CPL];
@@ -1101,7 +1146,10 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d, bool two_per_sm = false
   auto fit = [&](bool ded, int &st, int &smem) {
     st = (budget - fixed - (ded ? bs_bytes : 0)) / stage;
     if (st > 8) st = 8;
-    st -= st % SG;  // each group owns every SG-th stage
+    // a multiple of the warp groups: an odd count was measured no faster (the
+    // token loop is bound by the memory system's latency under load, which
+    // grows with the bytes in flight)
+    st -= st % SG;
     if (st < 2) st = 2;
     while (st * stage < std::max(ring_min, ded ? 0 : bs_bytes)) st += SG;
     smem = st * stage + (ded ? bs_bytes : 0) + fixed;
@@ -1134,8 +1182,8 @@ inline DecodePlan decode_tc_plan(const fla_attn_dims &d, bool two_per_sm = false
 inline bool decode_tc_shape_supported(const fla_attn_dims &d) { return decode_tc_plan(d).ok; }
 
 // SMs a single-request decode leaves idle for the merge grid behind it: one
-// per 16 merge warps (a warp per query row, at most 128 registers a thread).
-inline int decode_merge_reserve_sms(int hkv, int rows) { return (hkv * rows + 15) / 16; }
+// per 16 merge warps (two warps per query row, at most 128 registers a thread).
+inline int decode_merge_reserve_sms(int hkv, int rows) { return (2 * hkv * rows + 15) / 16; }
 
 // Tokens per work unit.  Single request: split every kv head's context into
 // floor((SMs - merge SMs) / hkv) units, so one wave covers the GPU and the
@@ -1209,7 +1257,7 @@ inline cudaError_t launch_merge(const dec::MergeParams &mp, int64_t nu_bound, bo
   const int64_t total = (int64_t)mp.n_req * mp.hkv * mp.rows;
   const bool lane = !prefer_rows && nu_bound <= kLaneMaxUnits;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = lane ? dim3((unsigned)((total + dec::kMergeLaneWarps - 1) / dec::kMergeLaneWarps))
+  cfg.gridDim = lane ? dim3((unsigned)((total + dec::kMergeLaneWarps / 2 - 1) / (dec::kMergeLaneWarps / 2)))
                      : dim3((unsigned)(mp.n_req * mp.hkv), (unsigned)mp.rows);
   cfg.blockDim = dim3(lane ? dec::kMergeLaneWarps * 32 : 4 * 32);
   // the four-warp kernel: this row's B slice plus the cross-warp combine buffer
