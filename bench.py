@@ -570,12 +570,14 @@ def run_legs(args, device, peaks, only=None):
         del Q, K, V, L, B
     # ---- ReBaseShared base projection fused with the LR build:
     #      [K_base | V_base | L] = X . [W_k | W_v | A_cat], one pass over X
+    # (the 16384-row case is the profiler-sized slice of the 70B one, run only when asked for)
     for leg, wname, rows in (("llama8b_prefill/rebase_kv_lr_build", "llama8b_prefill", None),
-                             ("llama70b_decode/rebase_kv_lr_build", "llama70b_decode", None)):
-        if not want(leg):
+                             ("llama70b_decode/rebase_kv_lr_build", "llama70b_decode", None),
+                             ("llama70b_decode/rebase_kv_lr_build_16k_rows", "llama70b_decode", 16384)):
+        if not want(leg) or (only is None and rows is not None):
             continue
         w = WORKLOADS[wname]
-        n = w.build_tokens
+        n = rows or w.build_tokens
         D, kv, lr = w.d_model, w.hkv * w.head_dim, w.n_agents * w.rank
         X, W = rnd((n, D)), rnd((D, 2 * kv + lr), D ** -0.5)
         K = torch.empty((n, w.hkv, w.head_dim), dtype=torch.bfloat16, device=device)
