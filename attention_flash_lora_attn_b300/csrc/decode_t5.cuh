@@ -16,8 +16,11 @@
 //   S^T  = K_tile . Q^T        M = 128 keys (one TMEM lane per key),
 //                              N = 64 query rows (A*G of them real)
 //   O^T += V_tile^T . P^T      M = d = 128, K = keys: V as an MN-major A
-//   OL^T+= L_tile^T . P^T      M = 128 L columns per MMA (every agent's r
-//                              columns), so the TMEM cost per row is 1 column
+//   OL^T+= L_tile^T . P^T      M = 128 L columns per MMA (a chunk of the
+//                              agents' r-column blocks), N = only the query
+//                              rows of the agents owning those columns (the
+//                              P^T operand starts at the chunk's first row),
+//                              so each chunk costs a few TMEM columns
 //   l                          row sums: each softmax thread adds its key's P
 //                              values into its own TMEM lane (64 columns, one
 //                              per query row); the 128 lanes are summed once,
@@ -72,6 +75,9 @@ struct Params {
   int32_t l_agent_stride, l_width, n_lbox, n_lchunk;
   int32_t unit_tokens, single_len, part_stride;
   int32_t nk, nv, vl_bytes;
+  // OL^T chunk c: query rows [ol_row0[c], ol_row0[c] + ol_rows[c]) (a multiple
+  // of 8, a multiple of 16) accumulated in TMEM columns kColOL + ol_col[c] + i
+  int32_t ol_row0[kMaxLChunks], ol_rows[kMaxLChunks], ol_col[kMaxLChunks];
   float scale_log2;
 };
 
@@ -233,6 +239,10 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
     if (lane == 0) {
       const uint32_t idesc_s = ptx::idesc_bf16_f32(kKeys, kN);                           // K, Q: K-major
       const uint32_t idesc_v = ptx::idesc_bf16_f32(kKeys, kN) | (1u << 15) | (1u << 16);  // V/L and P: MN-major
+      uint32_t idesc_ol[kMaxLChunks];
+#pragma unroll
+      for (int c = 0; c < kMaxLChunks; ++c)
+        idesc_ol[c] = ptx::idesc_bf16_f32(kKeys, c < p.n_lchunk ? p.ol_rows[c] : 16) | (1u << 15) | (1u << 16);
       const uint64_t d_q = ptx::smem_desc_k128(ptx::smem_u32(q_s));
       const uint64_t d_k = ptx::smem_desc_k128(ptx::smem_u32(k_s));
       const uint64_t d_p = ptx::smem_desc_mn128(ptx::smem_u32(p_s), 8192);
@@ -267,9 +277,11 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
             const uint32_t acc = (j > 0 || h > 0 || ks > 0) ? 1u : 0u;
             const uint64_t bP = ptx::desc_advance(d_p, (h * kHalf + ks * 16) * 128);
             ptx::tc_mma_f16(tmem + kColO, ptx::desc_advance(dv, ks * 2048), bP, idesc_v, acc);
-            for (int c = 0; c < p.n_lchunk; ++c)
-              ptx::tc_mma_f16(tmem + kColOL + c * kN, ptx::desc_advance(dl, c * 2 * kLBoxBytes + ks * 2048), bP,
-                              idesc_v, acc);
+#pragma unroll
+            for (int c = 0; c < kMaxLChunks; ++c)
+              if (c < p.n_lchunk)  // P^T from the chunk's first query row: 2 bytes a row within each key's 128
+                ptx::tc_mma_f16(tmem + kColOL + p.ol_col[c], ptx::desc_advance(dl, c * 2 * kLBoxBytes + ks * 2048),
+                                ptx::desc_advance(bP, p.ol_row0[c] * 2), idesc_ol[c], acc);
           }
           ptx::tc_commit(ve(st));
         }
@@ -376,8 +388,8 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
           }
           waited = true;
           ptx::tc_fence_after();
-          for (int reg = 0; reg < 2 + p.n_lchunk; ++reg) {
-            const uint32_t col = reg == 0 ? kColO : reg == 1 ? kColLs : kColOL + (reg - 2) * kN;
+          for (int reg = 0; reg < 2; ++reg) {
+            const uint32_t col = reg == 0 ? kColO : kColLs;
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
               uint32_t ov[32];
@@ -387,6 +399,29 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 #pragma unroll
               for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * f[hh * 32 + i]);
               ptx::tmem_st32(tmem + lane_base + col + hh * 32, ov);
+            }
+          }
+          // OL^T chunks: column i of chunk c holds row ol_row0[c] + i; chunks
+          // are scaled one after another (a 32-column load may reach into the
+          // next chunk, whose values are written back unchanged first)
+          for (int c = 0; c < p.n_lchunk; ++c) {
+            const int r0 = p.ol_row0[c], nr = p.ol_rows[c];
+            for (int hh = 0; hh * 32 < nr; ++hh) {
+              uint32_t ov[32];
+              ptx::tmem_st_wait();
+              ptx::tmem_ld32(tmem + lane_base + kColOL + p.ol_col[c] + hh * 32, ov);
+              ptx::tmem_ld_wait();
+              ptx::reg_fence32(ov);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                const int row = r0 + hh * 32 + i;
+                if (hh * 32 + i < nr) {
+                  const float mc = m_cur[row];
+                  const float fr = (mc == -INFINITY) ? 0.f : ptx::ex2(mc - m_new(row));
+                  ov[i] = __float_as_uint(__uint_as_float(ov[i]) * fr);
+                }
+              }
+              ptx::tmem_st32(tmem + lane_base + kColOL + p.ol_col[c] + hh * 32, ov);
             }
           }
           ptx::tmem_st_wait();
@@ -483,18 +518,22 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
         for (int c = 0; c < kN; ++c)
           if (c < p.rows) part[c * W + key] = __uint_as_float(ov[c]);
         for (int ch = 0; ch < p.n_lchunk; ++ch) {
-          ptx::tmem_ld32(tmem + lane_base + kColOL + ch * kN, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-          ptx::tmem_ld32(tmem + lane_base + kColOL + ch * kN + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+          // columns kColOL + ol_col[ch] + i hold rows ol_row0[ch] + i (the
+          // loads may reach into the next chunk, whose columns are not used here)
+          ptx::tmem_ld32(tmem + lane_base + kColOL + p.ol_col[ch], *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+          ptx::tmem_ld32(tmem + lane_base + kColOL + p.ol_col[ch] + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
           ptx::tmem_ld_wait();
           ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
           ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
           const int col = ch * kKeys + key;  // L column held by this lane
+          const int r0 = p.ol_row0[ch], nr = p.ol_rows[ch];
           if (col < p.l_width) {
 #pragma unroll
-            for (int c = 0; c < kN; ++c) {
-              if (c >= p.rows) break;
+            for (int i = 0; i < kN; ++i) {
+              const int c = r0 + i;
+              if (i >= nr || c >= p.rows) break;
               const int lo = (c / p.G) * p.l_agent_stride;
-              if (col >= lo && col < lo + p.r) part[c * W + D + col - lo] = __uint_as_float(ov[c]);
+              if (col >= lo && col < lo + p.r) part[c * W + D + col - lo] = __uint_as_float(ov[i]);
             }
           }
         }
@@ -530,6 +569,7 @@ decode_t5_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant_
 // ---------------------------------------------------------------------------
 struct DecodeT5Plan {
   int rows, l_width, n_lbox, n_lchunk, nk, nv, vl_bytes, smem_bytes, part_stride;
+  int ol_row0[dt5::kMaxLChunks], ol_rows[dt5::kMaxLChunks], ol_col[dt5::kMaxLChunks];
   bool ok;
 };
 
@@ -558,6 +598,28 @@ inline DecodeT5Plan decode_t5_plan(const fla_attn_dims &d) {
   if (nv >= 5 && fixed + 3 * dt5::kKBytes + (nv - 1) * vl_bytes + spare <= budget) {
     nk = 3;
     nv -= 1;
+  }
+  // OL^T chunk c (L columns [128c, 128c + 128)) only needs the query rows of
+  // the agents whose blocks it holds: rows [a_lo*G, (a_hi+1)*G), widened to a
+  // start on a multiple of 8 rows (16-byte operand offset) and a multiple of
+  // 16 rows (the MMA's N), inside the 64 rows of P^T
+  int col = 0;
+  for (int c = 0; c < n_lchunk; ++c) {
+    int lo_row = 0, hi_row = rows;
+    if (d.l_agent_stride != 0) {
+      const int a_lo = (c * dt5::kKeys) / d.rank;
+      const int a_hi = std::min(d.n_agents - 1, (c * dt5::kKeys + dt5::kKeys - 1) / d.rank);
+      lo_row = a_lo * G;
+      hi_row = std::min(rows, (a_hi + 1) * G);
+    }
+    int r0 = lo_row / 8 * 8;
+    int nr = (hi_row - r0 + 15) / 16 * 16;
+    if (nr < 16) nr = 16;
+    if (r0 + nr > dt5::kN) r0 = dt5::kN - nr;  // still covers [lo_row, hi_row)
+    pl.ol_row0[c] = r0;
+    pl.ol_rows[c] = nr;
+    pl.ol_col[c] = col;
+    col += nr;
   }
   pl.rows = rows; pl.l_width = l_width; pl.n_lbox = n_lbox; pl.n_lchunk = n_lchunk;
   pl.nk = nk; pl.nv = nv; pl.vl_bytes = vl_bytes;
@@ -642,6 +704,11 @@ inline fla_status decode_t5_launch(const fla_attn_dims &d, float scale, const vo
   prm.single_len = n_req == 1 ? (int)total_tokens : -1;
   prm.part_stride = pl.part_stride;
   prm.nk = pl.nk; prm.nv = pl.nv; prm.vl_bytes = pl.vl_bytes;
+  for (int c = 0; c < dt5::kMaxLChunks; ++c) {
+    prm.ol_row0[c] = c < pl.n_lchunk ? pl.ol_row0[c] : 0;
+    prm.ol_rows[c] = c < pl.n_lchunk ? pl.ol_rows[c] : 16;
+    prm.ol_col[c] = c < pl.n_lchunk ? pl.ol_col[c] : 0;
+  }
   prm.scale_log2 = scale * 1.4426950408889634f;
   const int64_t grid64 = units * d.hkv;
   if (grid64 > 0x7fffffffLL) {
