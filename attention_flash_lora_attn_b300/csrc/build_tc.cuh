@@ -288,6 +288,183 @@ build_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__
   ptx::cluster_sync_all();
 }
 
+// ---------------------------------------------------------------------------
+// The same GEMM on CTA pairs (cluster of 2, tcgen05 cta_group::2): a pair owns
+// 256 rows of X (128 per CTA) and a column tile; each MMA chunk (128 or 256
+// columns) is split into column halves, one in each CTA's shared memory, so a
+// CTA copies only half of the tile's W boxes per k-step and the W bytes each
+// SM loads per MMA flop halve.  The even CTA issues every MMA and commits the
+// stage releases and the finished accumulator to both CTAs; both CTAs' copies
+// count on the even CTA's full barriers.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+build_tc2_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA, const Params p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int a_bytes = kBM * kBK * 2;
+  const int stage_bytes = a_bytes + (p.tile_boxes / 2) * kBoxBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + p.stages * stage_bytes);
+  // bars: full[stages] | empty[stages] | acc_full | drain
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = ptx::cluster_ctarank();  // 0: the CTA that issues the MMAs
+  const int64_t pair_tile = blockIdx.x / 2;
+  const int nt = (int)(pair_tile % p.n_ntiles);
+  const int64_t m0 = (pair_tile / p.n_ntiles) * (2 * kBM) + rank * kBM;  // this CTA's rows
+  const int c0 = nt * p.tile_boxes * kBoxN;
+  // boxes of this tile, rounded up to an even count (zero-filled past N);
+  // MMA chunk 0 takes up to 4 of them (256 columns), chunk 1 the rest
+  int nb = min(p.tile_boxes, (p.N + kBoxN - 1) / kBoxN - nt * p.tile_boxes);
+  nb = (nb + 1) & ~1;
+  const int chunk0 = min(4, nb), chunk1 = nb - chunk0;
+  const int load_bytes = a_bytes + (nb / 2) * kBoxBytes;  // this CTA's copies per k-step
+  const int n_k = p.ksteps;
+  const uint32_t full0 = ptx::smem_u32(&bars[0]);
+  const uint32_t empty0 = ptx::smem_u32(&bars[p.stages]);
+  const uint32_t acc_full = ptx::smem_u32(&bars[2 * p.stages]);
+  const uint32_t drain = ptx::smem_u32(&bars[2 * p.stages + 1]);
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < p.stages; ++s) {
+      ptx::mbar_init(full0 + 8 * s, 1);
+      ptx::mbar_init(empty0 + 8 * s, 1);
+    }
+    ptx::mbar_init(acc_full, 1);
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc_pair(ptx::smem_u32(&s_tmem), p.tmem_cols);
+    ptx::tmem_relinquish_pair();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  // the peer signals this CTA's barriers: both initialisations first
+  ptx::cluster_sync_all();
+  ptx::tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t lead_full0 = ptx::mapa_cluster(full0, 0);
+
+  if (warp == 0) {
+    // ======================= TMA producer (both CTAs) =======================
+    if (lane == 0) {
+      ptx::prefetch_tmap(&tmX);
+      ptx::prefetch_tmap(&tmA);
+      int issued = 0;
+      for (int kt = 0; kt < n_k; ++kt) {
+        const int s = kt % p.stages;
+        if (kt >= p.stages && !ptx::mbar_wait_cluster(empty0 + 8 * s, ((kt / p.stages) & 1) ^ 1)) {
+          set_device_error(kErrBuildEmptyWait);
+          s_abort = 1;
+          break;
+        }
+        if (*(volatile int *)&s_abort) break;
+        const uint32_t fb = lead_full0 + 8 * s;  // the even CTA's full barrier counts both CTAs' bytes
+        if (rank == 0) ptx::mbar_arrive_expect_tx(full0 + 8 * s, 2 * load_bytes);
+        const uint32_t sa = ptx::smem_u32(smem + s * stage_bytes);
+        const int k = kt * kBK;
+        ptx::tma_load_2d_pair(sa, &tmX, k, (int32_t)m0, fb);
+        // this CTA's column half of each chunk
+        for (int b = 0; b < chunk0 / 2; ++b)
+          ptx::tma_load_2d_pair(sa + a_bytes + b * kBoxBytes, &tmA, c0 + (rank * (chunk0 / 2) + b) * kBoxN, k, fb);
+        for (int b = 0; b < chunk1 / 2; ++b)
+          ptx::tma_load_2d_pair(sa + a_bytes + (chunk0 / 2 + b) * kBoxBytes, &tmA,
+                                c0 + (chunk0 + rank * (chunk1 / 2) + b) * kBoxN, k, fb);
+        ++issued;
+      }
+      // the even CTA's full barriers also count the peer's copies: leave none in flight
+      if (rank == 0)
+        for (int k = 0; k < p.stages && k < issued; ++k) {
+          const int kt = issued - 1 - k;
+          ptx::mbar_wait_cluster(full0 + 8 * (kt % p.stages), (kt / p.stages) & 1);
+        }
+    }
+  } else if (warp == 1) {
+    // ======================= MMA issuer (even CTA) =======================
+    if (lane == 0 && rank == 0) {
+      const uint32_t idesc0 = ptx::idesc_bf16_f32(2 * kBM, chunk0 * kBoxN) | (1u << 16);  // B MN-major
+      const uint32_t idesc1 = ptx::idesc_bf16_f32(2 * kBM, (chunk1 > 0 ? chunk1 : 2) * kBoxN) | (1u << 16);
+      const uint64_t d_a = ptx::smem_desc_k128(ptx::smem_u32(smem));
+      const uint64_t d_b = ptx::smem_desc_mn128(ptx::smem_u32(smem) + a_bytes, kBoxBytes);
+      const uint32_t empty_peer0 = ptx::mapa_cluster(empty0, 1);
+      const uint32_t empty_own0 = ptx::mapa_cluster(empty0, 0);
+      bool ok = true;
+      for (int kt = 0; kt < n_k; ++kt) {
+        const int s = kt % p.stages;
+        if (!ptx::mbar_wait_cluster(full0 + 8 * s, (kt / p.stages) & 1)) {
+          set_device_error(kErrBuildFullWait);
+          s_abort = 1;
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint64_t da = ptx::desc_advance(d_a, s * stage_bytes);
+        const uint64_t db = ptx::desc_advance(d_b, s * stage_bytes);
+#pragma unroll
+        for (int k16 = 0; k16 < kBK / 16; ++k16) {
+          const uint32_t acc = (kt > 0 || k16 > 0) ? 1u : 0u;
+          ptx::tc_mma_f16_pair(tmem, ptx::desc_advance(da, k16 * 32), ptx::desc_advance(db, k16 * 2048), idesc0, acc);
+          if (chunk1 > 0)
+            ptx::tc_mma_f16_pair(tmem + chunk0 * kBoxN, ptx::desc_advance(da, k16 * 32),
+                                 ptx::desc_advance(db, (chunk0 / 2) * kBoxBytes + k16 * 2048), idesc1, acc);
+        }
+        // stage s is free in both CTAs once these MMAs have read it
+        ptx::tc_commit_pair(empty_own0 + 8 * s);
+        ptx::tc_commit_pair(empty_peer0 + 8 * s);
+      }
+      if (ok) {
+        ptx::tc_commit_pair(ptx::mapa_cluster(acc_full, 0));
+        ptx::tc_commit_pair(ptx::mapa_cluster(acc_full, 1));
+      } else {
+        ptx::tc_commit_pair(ptx::mapa_cluster(drain, 0));
+        ptx::mbar_wait(drain, 0);
+      }
+    }
+  } else {
+    // ======================= epilogue (warps 2..5, both CTAs) =======================
+    const int quarter = warp & 3;  // TMEM lanes [32*quarter, 32*quarter + 32)
+    const int64_t row = m0 + quarter * 32 + lane;
+    bool ready = false;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+      if (ptx::mbar_try_wait_cluster(acc_full, 0)) { ready = true; break; }
+      if (*(volatile int *)&s_abort) break;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        set_device_error(kErrBuildAccWait);
+        s_abort = 1;
+        break;
+      }
+    }
+    if (ready) {
+      ptx::tc_fence_after();
+      const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+      const int ncols = min(nb * kBoxN, p.N - c0);  // multiple of 32
+      for (int c = 0; c < ncols; c += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tl + c, v);
+        ptx::tmem_ld_wait();
+        if (row < p.n) {
+          uint4 out[4];
+          uint32_t *o = reinterpret_cast<uint32_t *>(out);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            o[i] = ptx::pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          uint4 *dst = reinterpret_cast<uint4 *>(out_ptr(p, row, c0 + c));  // 32 columns, one segment
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = out[i];
+        }
+      }
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  // neither CTA frees the pair's TMEM (or leaves) while the other still works
+  ptx::cluster_sync_all();
+  if (warp == 1) ptx::tmem_dealloc_pair(tmem, p.tmem_cols);
+}
+
 }  // namespace bld
 
 // ---------------------------------------------------------------------------
@@ -375,6 +552,34 @@ inline BuildPlan build_tc_plan(int64_t n, int d_model, int n_cols, int sms, int 
   return best;
 }
 
+// Plan of the CTA-pair kernel: column tiles of an even number of boxes (<= 8;
+// a tile whose box count is odd copies one zero-filled box past column N), each
+// CTA holding half of every tile's boxes per stage.
+inline BuildPlan build_tc2_plan(int d_model, int n_cols) {
+  BuildPlan pl{};
+  pl.ok = false;
+  if (d_model < bld::kBK || d_model % bld::kBK != 0 || n_cols % 32 != 0 || n_cols < 32) return pl;
+  const int boxes = (n_cols + bld::kBoxN - 1) / bld::kBoxN;
+  const int nt = (boxes + 7) / 8;
+  int bpt = (boxes + nt - 1) / nt;
+  bpt = (bpt + 1) & ~1;
+  pl.tile_boxes = bpt;
+  pl.n_ntiles = (boxes + bpt - 1) / bpt;
+  pl.split = 1;
+  pl.ksteps = d_model / bld::kBK;
+  pl.red_pitch = 0;
+  const int stage = bld::kBM * bld::kBK * 2 + (bpt / 2) * bld::kBoxBytes;
+  const int st = std::min((bld::kSmemBudget - 1024 - 128) / stage, 8);
+  if (st < 2 || build_smem_bytes(st, stage) > 227 * 1024) return pl;
+  pl.stages = st;
+  pl.smem_bytes = build_smem_bytes(st, stage);
+  uint32_t cols = 32;
+  while ((int)cols < bpt * bld::kBoxN) cols <<= 1;
+  pl.tmem_cols = cols;
+  pl.ok = true;
+  return pl;
+}
+
 // Largest cluster (16, else 8) of this kernel that the device can place with
 // `smem` bytes per CTA; cached per device and shared-memory size.
 inline int build_max_cluster(int smem) {
@@ -443,6 +648,16 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *W, con
     const BuildPlan p16 = build_tc_plan(n, d_model, n_cols, sms, 16);
     if (p16.split == 16 && build_max_cluster(p16.smem_bytes) >= 16) pl = p16;
   }
+  // Without a split of d_model the rows fill the GPU: CTA pairs (256 rows,
+  // half of the W boxes per CTA) do the same work with half the W copies.
+  bool pair = false;
+  if (pl.split == 1 && n > bld::kBM) {
+    const BuildPlan p2 = build_tc2_plan(d_model, n_cols);
+    if (p2.ok) {
+      pl = p2;
+      pair = true;
+    }
+  }
   PFN_encodeTiled enc = get_encode_tiled();
   if (!enc) {
     build_tc_err() = "cuTensorMapEncodeTiled is not available from the driver";
@@ -492,16 +707,38 @@ inline fla_status build_tc_launch(const void *X, int64_t ldx, const void *W, con
   prm.ksteps = pl.ksteps;
   prm.red_pitch = pl.red_pitch;
   prm.tmem_cols = pl.tmem_cols;
-  const void *fn = reinterpret_cast<const void *>(bld::build_tc_kernel);
+  const void *fn = pair ? reinterpret_cast<const void *>(bld::build_tc2_kernel)
+                        : reinterpret_cast<const void *>(bld::build_tc_kernel);
   cudaError_t e = ensure_dynamic_smem(fn, pl.smem_bytes);
   if (e != cudaSuccess) {
     build_tc_err() = cudaGetErrorString(e);
     return FLA_ERR_CUDA;
   }
-  const int64_t grid = (n + bld::kBM - 1) / bld::kBM * pl.n_ntiles * pl.split;
+  const int64_t grid = pair ? (n + 2 * bld::kBM - 1) / (2 * bld::kBM) * pl.n_ntiles * 2
+                            : (n + bld::kBM - 1) / bld::kBM * pl.n_ntiles * pl.split;
   if (grid > 0x7fffffffLL) {
     build_tc_err() = "n_tokens too large";
     return FLA_ERR_UNSUPPORTED;
+  }
+  if (pair) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(bld::kThreads);
+    cfg.dynamicSmemBytes = pl.smem_bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, bld::build_tc2_kernel, mX, mW, prm);
+    if (e != cudaSuccess) {
+      build_tc_err() = cudaGetErrorString(e);
+      return FLA_ERR_CUDA;
+    }
+    return FLA_OK;
   }
   if (pl.split == 1) {
     bld::build_tc_kernel<<<(unsigned)grid, bld::kThreads, pl.smem_bytes, s>>>(mX, mW, prm);

@@ -348,6 +348,27 @@ def test_lr_build_tensor_kernel(case):
     assert _rel_l2(L.double().cpu().numpy(), ref) <= BUILD_RTOL_L2
 
 
+# Enough rows that the tile count exceeds half the SMs: the plan takes the
+# CTA-pair kernel (256 rows per pair, each CTA copying half of the W boxes).
+# Ragged row tails (the odd CTA of the last pair past the end), odd box counts
+# (a zero-filled box completes the pair), partial boxes and several column tiles.
+PAIR_BUILD = [(10000, 256, 320), (9700, 128, 96), (2000, 512, 2368), (19200, 192, 64), (12345, 64, 512)]
+
+
+@pytest.mark.parametrize("case", PAIR_BUILD, ids=["n320-odd-boxes", "n96-partial", "n2368-5-tiles", "n64", "n512"])
+def test_lr_build_cta_pairs(case):
+    n, D, N = case
+    x = make_build_inputs(n, D, 1, N, torch.bfloat16, seed=9)
+    L = _fla().lr_cache_build(x["X"].cuda(), x["A_cat"].cuda(), kernel="tcgen05")
+    ref = oracle.lr_cache_build(x["X"], x["A_cat"])
+    got = L.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    assert _rel_l2(got, ref) <= BUILD_RTOL_L2
+    # every row, the last ones included, on its own
+    per_row = np.linalg.norm(got - ref, axis=1) / np.maximum(np.linalg.norm(ref, axis=1), 1e-30)
+    assert per_row.max() <= 4 * BUILD_RTOL_L2
+
+
 def test_lr_build_strided_output_leaves_other_columns():
     x = make_build_inputs(200, 512, 2, 32, torch.bfloat16, seed=6)
     L = torch.full((200, 100), 7.0, dtype=torch.bfloat16, device="cuda")
@@ -419,6 +440,15 @@ def test_rebase_projection_llama8b_chunk_full():
     _rebase_check(x, K, V, Ls, w.hkv, w.head_dim)
     Lc = L.double().cpu().numpy()
     assert (Lc[:, :8] == 7).all() and (Lc[:, 8 + w.n_agents * w.rank:] == 7).all()
+
+
+def test_rebase_projection_cta_pairs():
+    """Three output segments through the CTA-pair kernel: 4000 rows, 512 + 512 + 96 columns in three tiles."""
+    n, D, hkv, d, A, r = 4000, 256, 4, 128, 6, 16
+    x = make_rebase_inputs(n, D, hkv, d, A, r, torch.bfloat16, seed=13)
+    W = torch.cat([x["W_k"], x["W_v"], x["A_cat"]], dim=1).cuda()
+    K, V, L = _fla().rebase_kv_lr_build(x["X"].cuda(), W, hkv=hkv, head_dim=d, n_agents=A, rank=r, kernel="tcgen05")
+    _rebase_check(x, K, V, L, hkv, d)
 
 
 def test_rebase_projection_llama70b_shape_sampled_rows():
