@@ -194,6 +194,20 @@ __device__ __forceinline__ uint64_t smem_desc_mn128(uint32_t saddr, uint32_t box
   return d;
 }
 
+// Shared-memory matrix descriptor for an MN-major operand in the 64-byte
+// swizzled layout a TMA box of 32 columns (64 bytes) x K rows produces:
+// 512-byte swizzle atoms of 8 rows, K advances by 64 bytes per row.
+// `group_stride`: bytes between consecutive 32-column groups.
+__device__ __forceinline__ uint64_t smem_desc_mn64(uint32_t saddr, uint32_t group_stride) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((group_stride >> 4) & 0x3FFF) << 16;  // leading byte offset: next 32-column group
+  d |= (uint64_t)(512 >> 4) << 32;                       // stride byte offset: next 8 rows of K
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;                                // 64-byte swizzle
+  return d;
+}
+
 // A matrix descriptor whose start address is `bytes` (a multiple of 16)
 // further on.  The start-address field is the low 14 bits (address >> 4) and
 // every shared-memory address of a CTA is below 256 KB, so the addition never
@@ -272,6 +286,14 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
       "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
@@ -307,10 +329,30 @@ __device__ __forceinline__ void tc_mma_f16_pair(uint32_t d_tmem, uint64_t a_desc
       : "memory");
 }
 
+// The same with A in tensor memory (each CTA's 128 rows at address a_tmem of its own TMEM).
+__device__ __forceinline__ void tc_mma_f16_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                                   uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on the mbarrier at shared::cluster address `bar` (either CTA of the
 // pair) once every pair MMA issued so far by this thread has completed.
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// The same arrival on the mbarrier at shared::cta address `bar` in every CTA
+// of the cluster whose bit is set in `cta_mask` (one instruction for both CTAs
+// of a pair).
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
 }
 
 // TMA tile load into this CTA's shared memory whose completion is counted on
@@ -324,16 +366,34 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *m, int32_t x, int32_t y, int32_t z,
+                                                 uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+// Arrive (release at cluster scope) on the mbarrier at shared::cluster address
+// `caddr`, in this CTA or another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
 // try_wait with cluster-scope acquire (the phase may be completed by copies
-// and commits issued from the peer CTA).
+// and commits issued from the peer CTA).  The thread is suspended in hardware
+// until the phase completes or about 1 ms has passed, instead of spinning: a
+// polling producer or MMA thread would otherwise take issue slots from the
+// softmax warp that shares its SM sub-partition.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t done;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(done)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(1000000u)
       : "memory");
   return done != 0;
 }
@@ -344,6 +404,32 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity)
   while (true) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Arrive without release semantics on the mbarrier at shared::cluster address
+// `caddr`.  For signalling tensor-memory data: the writer's tcgen05.wait::st
+// has completed its stores and tcgen05.fence::before_thread_sync orders them
+// before this arrive; the reader issues tcgen05.fence::after_thread_sync after
+// its wait.  A release at cluster scope would also drain every other memory
+// operation of the thread, which costs far more than the signal itself.
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+// Cluster-scope counterpart of mbar_wait_or_abort.
+__device__ __forceinline__ bool mbar_wait_cluster_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                                           uint32_t err) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      set_device_error(err);
+      *abort_flag = 1;
+      return false;
+    }
   }
 }
 
