@@ -22,7 +22,6 @@
 #include "build_tc.cuh"
 #include "prefill_mma.cuh"
 #include "prefill_tc.cuh"
-#include "prefill_pair.cuh"
 #include "expand.cuh"
 
 namespace {
@@ -324,7 +323,7 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
   if (k == FLA_KERNEL_TENSOR && !tc5 && !mma)
     return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside both tensor-core kernels");
   if (tc5 && (k == FLA_KERNEL_AUTO || k == FLA_KERNEL_TENSOR || k == FLA_KERNEL_TCGEN05)) {
-    st = fla::prefill_pair_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, s);
+    st = fla::prefill_tcgen05_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, s);
     if (st != FLA_OK) return fail(st, "prefill (tcgen05): %s", fla::prefill_tcgen05_last_error());
     return check_launch("prefill (tcgen05)");
   }
