@@ -420,15 +420,20 @@ def run_ours(args, ws, rank, local):
     return line
 
 
-def _median_launch_s(fn, reps, stream, flush=None):
+def _median_launch_s(fn, reps, stream, flush=None, settle=False):
     """Median device time of one fn() call over reps replays.
 
     fn is captured once into a CUDA graph, so the events bracket only the
     kernels the call enqueues (no host-side argument handling); an optional
-    L2 flush runs between replays, outside the events.
+    L2 flush runs between replays, outside the events.  settle: start after
+    one idle second, so that a tensor-bound leg is not measured under the power
+    cap its predecessors in the same process pushed the GPU into.
     """
     import torch
 
+    if settle:
+        torch.cuda.synchronize()
+        time.sleep(1.0)
     with torch.cuda.stream(stream):
         for _ in range(3):
             fn()
@@ -497,7 +502,7 @@ def run_legs(args, device, peaks, only=None):
         B = rnd((A, r, w.hkv * w.head_dim), 0.02)
         O = torch.empty((A, c, w.hq, w.head_dim), dtype=torch.float32, device=device)
         t = _median_launch_s(lambda: fla.flash_lora_attn_prefill(Q, K, V, L, B, n0, rank=r, O=O),
-                             max(3, reps // 4), stream, flush)
+                             max(3, reps // 4), stream, flush, settle=True)
         # causal: query p sees n0+p+1 keys; QK^T and PV over d, PL over r, (PL)B once per query
         keys = sum(n0 + p + 1 for p in range(c))
         flops = A * w.hq * keys * (4 * w.head_dim + 2 * r) + A * c * w.hq * 2 * r * w.head_dim
@@ -585,7 +590,7 @@ def run_legs(args, device, peaks, only=None):
         t = _median_launch_s(lambda: fla.rebase_kv_lr_build(X, W, hkv=w.hkv, head_dim=w.head_dim,
                                                             n_agents=w.n_agents, rank=w.rank, K_base=K, V_base=V,
                                                             L=L), max(3, reps // 2), stream,
-                             flush if n * D * 2 < L2_BYTES else None)
+                             flush if n * D * 2 < L2_BYTES else None, settle=True)
         flops, byts = 2 * n * D * (2 * kv + lr), (n * D + D * (2 * kv + lr) + n * (2 * kv + lr)) * 2
         out[leg] = {
             "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
@@ -601,7 +606,8 @@ def run_legs(args, device, peaks, only=None):
         n, D, Nc = rows, w.d_model, w.n_agents * w.rank
         X, A_cat = rnd((n, D)), rnd((D, Nc), D ** -0.5)
         L = torch.empty((n, Nc), dtype=torch.bfloat16, device=device)
-        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_cat, L, n_agents=w.n_agents), max(3, reps // 2), stream)
+        t = _median_launch_s(lambda: fla.lr_cache_build(X, A_cat, L, n_agents=w.n_agents), max(3, reps // 2), stream,
+                             settle=True)
         flops, byts = 2 * n * D * Nc, (n * D + Nc * D + n * Nc) * 2
         out[leg] = {
             "us": t * 1e6, "tflops": flops / t / 1e12, "tensor_frac": flops / t / 1e12 / peaks["bf16_tflops"],
