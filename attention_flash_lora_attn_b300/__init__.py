@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     lora_value_expand,
     lr_cache_build,
     rebase_kv_lr_build,
+    selftest_bounded_wait,
     version,
 )
 

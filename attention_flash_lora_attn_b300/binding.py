@@ -28,7 +28,8 @@ STATUS = {0: "FLA_OK", 1: "FLA_ERR_INVALID_ARG", 2: "FLA_ERR_UNSUPPORTED", 3: "F
 EXPORTED = ("lr_cache_build", "flash_lora_attn_decode_workspace_size", "flash_lora_attn_decode",
             "flash_lora_attn_prefill_workspace_size", "flash_lora_attn_prefill", "fla_status_string",
             "fla_last_error", "fla_device_error", "fla_version", "flash_lora_attn_decode_noalloc",
-            "lora_value_expand", "flash_lora_attn_decode_host_io", "rebase_kv_lr_build")
+            "lora_value_expand", "flash_lora_attn_decode_host_io", "rebase_kv_lr_build",
+            "fla_selftest_bounded_wait")
 
 
 class FlaError(RuntimeError):
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.flash_lora_attn_decode_host_io.argtypes = [dims_p, vp, vp, vp, vp, vp, vp, vp, i32, i64, vp, vp, vp,
                                                        sz, vp]
         lib.flash_lora_attn_decode_host_io.restype = ctypes.c_int
+        lib.fla_selftest_bounded_wait.argtypes = [ctypes.c_uint64, vp, vp]
+        lib.fla_selftest_bounded_wait.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -414,6 +417,18 @@ def device_error() -> int:
     code = ctypes.c_uint32(0)
     _check(lib.fla_device_error(ctypes.byref(code)))
     return code.value
+
+
+def selftest_bounded_wait(limit_ns: int, stream=None) -> dict:
+    """Runs the bounded-wait self-test (a wait that nothing completes, limited to
+    limit_ns) and returns what the kernel observed plus the device error code it
+    left (read and cleared)."""
+    lib = load_library()
+    out = torch.zeros(3, dtype=torch.int64, device="cuda")
+    _check(lib.fla_selftest_bounded_wait(int(limit_ns), out.data_ptr(), _stream_ptr(stream)))
+    code = device_error()  # synchronises
+    o = out.cpu().tolist()
+    return {"timed_out": bool(o[0]), "peer_left_on_abort": bool(o[1]), "wait_ns": int(o[2]), "device_error": code}
 
 
 def version() -> str:

@@ -117,6 +117,34 @@ void launch_simt_attn(const fla::SimtAttnParams &p, int64_t rows, cudaStream_t s
   fla::simt_attn_kernel<T><<<(unsigned)rows, fla::kSimtWarps * 32, 0, s>>>(p);
 }
 
+// The bounded-wait path every pipeline kernel relies on, run on purpose:
+// warp 0 waits on an mbarrier no one arrives on, with a limit of limit_ns; on
+// timeout the helper records kErrSelfTestWait and raises the CTA's abort flag.
+// Warp 1 waits on a second such barrier with the kernels' 2 s limit and must
+// leave through the abort flag instead.  out[0] = 1 if warp 0's wait ran out,
+// out[1] = 1 if warp 1 left on the abort flag, out[2] = warp 0's wait in ns.
+__global__ void selftest_bounded_wait_kernel(uint64_t limit_ns, unsigned long long *out) {
+  __shared__ __align__(8) uint64_t bars[2];
+  __shared__ volatile int s_abort;
+  const uint32_t b0 = fla::ptx::smem_u32(&bars[0]), b1 = fla::ptx::smem_u32(&bars[1]);
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    fla::ptx::mbar_init(b0, 1);
+    fla::ptx::mbar_init(b1, 1);
+    fla::ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint64_t t0 = fla::globaltimer_ns();
+    const bool ok = fla::ptx::mbar_wait_or_abort(b0, 0, &s_abort, fla::kErrSelfTestWait, limit_ns);
+    out[0] = ok ? 0ull : 1ull;
+    out[2] = fla::globaltimer_ns() - t0;
+  } else if (threadIdx.x == 32) {
+    const bool ok = fla::ptx::mbar_wait_or_abort(b1, 0, &s_abort, fla::kErrSelfTestWait);
+    out[1] = (!ok && s_abort) ? 1ull : 0ull;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -136,6 +164,15 @@ const char *fla_status_string(fla_status s) {
 }
 
 const char *fla_last_error(void) { return g_last_error.c_str(); }
+
+fla_status fla_selftest_bounded_wait(uint64_t limit_ns, unsigned long long *out, fla_stream_t stream) {
+  g_last_error.clear();
+  if (!out) return fail(FLA_ERR_INVALID_ARG, "out is NULL");
+  if (limit_ns == 0 || limit_ns > fla::kWaitLimitNs)
+    return fail(FLA_ERR_INVALID_ARG, "limit_ns must be in (0, %llu]", (unsigned long long)fla::kWaitLimitNs);
+  selftest_bounded_wait_kernel<<<1, 64, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns, out);
+  return check_launch("fla_selftest_bounded_wait");
+}
 
 fla_status fla_device_error(uint32_t *code) {
   if (!code) return fail(FLA_ERR_INVALID_ARG, "code is NULL");

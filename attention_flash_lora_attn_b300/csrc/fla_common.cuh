@@ -24,6 +24,7 @@ enum DeviceErrorCode : uint32_t {
   kErrBuildAccWait = 0x203,     // LR build epilogue: accumulator never committed
   kErrBuildClusterWait = 0x204, // LR build split-K: a peer CTA never published its partial / finished reading
   kErrPrefillWait = 0x301,      // prefill: any pipeline wait
+  kErrSelfTestWait = 0x401,     // fla_selftest_bounded_wait: the wait it was asked to let run out
 };
 
 __device__ __forceinline__ void set_device_error(uint32_t code) {

@@ -63,13 +63,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
 // *abort_flag; on its own timeout it records `err` in the device error word
 // and raises the flag.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                                   uint32_t err) {
+                                                   uint32_t err, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       set_device_error(err);
       *abort_flag = 1;
       return false;

@@ -328,6 +328,23 @@ FLA_API const char *fla_last_error(void);
  * itself fails. */
 FLA_API fla_status fla_device_error(uint32_t *code);
 
+/* Self-test of the bounded waits (failure detection without a fault).
+ *
+ * Launches one CTA on `stream` whose warp 0 waits on an mbarrier that no one
+ * arrives on, through the same bounded-wait helper every pipeline kernel uses,
+ * with a limit of limit_ns nanoseconds; when it runs out the helper records
+ * code 0x401 in the device error word and raises the CTA's abort flag.  Warp 1
+ * waits on a second such barrier with the kernels' own 2 s limit and leaves
+ * through that flag.  No fault, trap or hang: the CTA returns and the context
+ * stays usable.
+ *   limit_ns  (0, 2e9].
+ *   out       device memory, 3 x uint64, written by the kernel: out[0] = 1 if
+ *             warp 0's wait ran out, out[1] = 1 if warp 1 left on the abort
+ *             flag, out[2] = warp 0's wait in nanoseconds.
+ * Read (and clear) the code with fla_device_error() afterwards.  Errors:
+ * INVALID_ARG (out NULL, limit out of range), CUDA (launch failure). */
+FLA_API fla_status fla_selftest_bounded_wait(uint64_t limit_ns, unsigned long long *out, fla_stream_t stream);
+
 /* Library version, e.g. "0.1.0". */
 FLA_API const char *fla_version(void);
 
