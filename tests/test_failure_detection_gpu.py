@@ -45,8 +45,8 @@ def test_a_wait_nothing_completes_times_out_and_reports(fla, limit_ms):
 
 
 def test_the_context_is_usable_after_a_timeout(fla):
-    fla.selftest_bounded_wait(2_000_000)
-    assert fla.device_error() == SELFTEST_CODE
+    r = fla.selftest_bounded_wait(2_000_000)
+    assert r["timed_out"] and r["device_error"] == SELFTEST_CODE, r
     w = WORKLOADS["tiny_decode"]
     x = make_decode_inputs(w, seed=3)
     d = {k: v.cuda() for k, v in x.items()}
