@@ -328,15 +328,17 @@ fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void *Q, cons
 
 // ---------------------------------------------------------------------------
 size_t flash_lora_attn_prefill_workspace_size(const fla_attn_dims *dims, int32_t chunk, int64_t n0) {
-  (void)dims; (void)chunk; (void)n0;
-  return 0;
+  float scale = 0.f;
+  if (!dims || check_dims(dims, &scale) != FLA_OK || chunk <= 0 || n0 < 0) return 0;
+  if (dims->kernel == FLA_KERNEL_SIMT || dims->kernel == FLA_KERNEL_MMA_SYNC) return 0;
+  const fla::PrefillTcgen05Plan pl = fla::prefill_tcgen05_plan(*dims, chunk, n0);
+  return pl.ok ? pl.part_bytes : 0;
 }
 
 fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, const void *K_base,
                                    const void *V_base, const void *L, const void *B, int64_t n0,
                                    int32_t chunk, float *O, void *workspace, size_t workspace_bytes,
                                    fla_stream_t stream) {
-  (void)workspace; (void)workspace_bytes;
   g_last_error.clear();
   float scale = 0.f;
   fla_status st = check_dims(dims, &scale);
@@ -348,7 +350,7 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool align_tc = aligned16(Q) && aligned16(K_base) && aligned16(V_base) && aligned16(L) &&
                         aligned16(B) && aligned16(O) && (dims->l_row_stride % 8 == 0);
-  const bool tc5 = align_tc && fla::prefill_tcgen05_plan(*dims, chunk).ok;
+  const bool tc5 = align_tc && fla::prefill_tcgen05_plan(*dims, chunk, n0).ok;
   const bool mma = align_tc && fla::prefill_tc_shape_supported(*dims);
   const int32_t k = dims->kernel;
   if (k == FLA_KERNEL_TCGEN05 && !tc5)
@@ -360,7 +362,8 @@ fla_status flash_lora_attn_prefill(const fla_attn_dims *dims, const void *Q, con
   if (k == FLA_KERNEL_TENSOR && !tc5 && !mma)
     return fail(FLA_ERR_UNSUPPORTED, "prefill: shape/alignment outside both tensor-core kernels");
   if (tc5 && (k == FLA_KERNEL_AUTO || k == FLA_KERNEL_TENSOR || k == FLA_KERNEL_TCGEN05)) {
-    st = fla::prefill_tcgen05_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, s);
+    st = fla::prefill_tcgen05_launch(*dims, scale, Q, K_base, V_base, L, B, n0, chunk, O, workspace, workspace_bytes,
+                                     s);
     if (st != FLA_OK) return fail(st, "prefill (tcgen05): %s", fla::prefill_tcgen05_last_error());
     return check_launch("prefill (tcgen05)");
   }

@@ -77,6 +77,19 @@ struct Params {
   int32_t l_agent_stride;
   int32_t nk, nv;  // depths of the K ring and of the [V | L] ring
   float scale_log2;
+  // Work items, in launch order: n_full pairs that run their whole key range,
+  // then n_split pairs run as two items each, one per half of their key tiles,
+  // whose unnormalised rows go to `part` (see PrefillPartRecord below)
+  int32_t n_qbp, n_full, n_split;
+  float *part;
+};
+
+// A half-range item's record of one query row: O and OL accumulated against
+// the running max m (log2 units of scaled scores), the row sum l against the
+// same max.  Records: [split pair][half][CTA rank][row], floats.
+template <int D>
+struct PartRec {
+  static constexpr int kFloats = D + 64 + 4;  // O[D], OL[64], m, l, 2 pad (16-byte aligned records)
 };
 
 template <int D>
@@ -122,15 +135,23 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = ptx::cluster_ctarank();  // 0: the CTA that issues the MMAs
-  const int pr = (int)(blockIdx.x >> 1);
+  const int item = (int)(blockIdx.x >> 1);
+  int pr = item, part_half = -1;  // -1: the whole key range
+  if (item >= p.n_full) {
+    pr = p.n_full + (item - p.n_full) / 2;
+    part_half = (item - p.n_full) & 1;
+  }
   const int head = pr % p.hkv;
-  const int n_qbp = (int)(gridDim.x >> 1) / p.hkv;
-  const int qbp = n_qbp - 1 - pr / p.hkv;  // late chunk blocks (most keys) first
+  const int qbp = p.n_qbp - 1 - pr / p.hkv;  // late chunk blocks (most keys) first
   const int p0 = (2 * qbp + (int)rank) * p.QB;
   // both CTAs run the tiles of the pair's later block; the earlier block's
   // rows see the extra keys masked
   const int64_t n_keys = p.n0 + min(p.chunk, (2 * qbp + 2) * p.QB);
-  const int n = (int)((n_keys + kT - 1) / kT);
+  const int n_all = (int)((n_keys + kT - 1) / kT);
+  // this item's key tiles [tb, tb + n)
+  const int tb = part_half == 1 ? n_all / 2 : 0;
+  const int n = part_half < 0 ? n_all : (part_half == 0 ? n_all / 2 : n_all - n_all / 2);
+  const bool full = part_half < 0;
   const int64_t causal_from = p.n0 + p0;
 
   const uint32_t bar0 = ptx::smem_u32(bars);
@@ -211,13 +232,13 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         const uint32_t fb = lead(kf(st));
 #pragma unroll
         for (int b = 0; b < D / 64; ++b)
-          ptx::tma_load_3d_pair(dst + b * kKBox, &tmK, b * 64, head, j * kT + (int)rank * (kT / 2), fb);
+          ptx::tma_load_3d_pair(dst + b * kKBox, &tmK, b * 64, head, (tb + j) * kT + (int)rank * (kT / 2), fb);
         k_issued = j + 1;
       }
       // this CTA's half of the head's B_cat rows, into the K ring once the
       // last S MMA (hence every S MMA) has finished with it
-      if (ok) ok = wait_ab(ke((n - 1) % p.nk), ((n - 1) / p.nk) & 1, &s_abort);
-      if (ok) {
+      if (ok && full) ok = wait_ab(ke((n - 1) % p.nk), ((n - 1) / p.nk) & 1, &s_abort);
+      if (ok && full) {
         if (rank == 0) ptx::mbar_arrive_expect_tx(bfull, 2 * kBBytes);
         ptx::tma_load_2d_pair(ptx::smem_u32(k_s), &tmB, head * D + (int)rank * VH, 0, lead(bfull));
         b_issued = true;
@@ -240,9 +261,9 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         for (int gi = 0; gi < kGroups; ++gi) {
           const int g = (int)rank * kGroups + gi;  // group of [V | L]
           if (g < D / 32)
-            ptx::tma_load_3d_pair(dst + gi * kGroupBytes, &tmV, 32 * g, head, j * kT, fb);
+            ptx::tma_load_3d_pair(dst + gi * kGroupBytes, &tmV, 32 * g, head, (tb + j) * kT, fb);
           else
-            ptx::tma_load_2d_pair(dst + gi * kGroupBytes, &tmL, 32 * (g - D / 32), j * kT, fb);
+            ptx::tma_load_2d_pair(dst + gi * kGroupBytes, &tmL, 32 * (g - D / 32), (tb + j) * kT, fb);
         }
         v_issued = j + 1;
       }
@@ -307,9 +328,10 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
         commit_both(pvdone(b));
       }
       // O += [OL_hi | OL_lo] . [B_cat ; B_cat]   (K = 2 x 64), signalled as "tile n"
-      if (ok) ok = wait_ab(pfull(n % kNBuf), (n / kNBuf) & 1, &s_abort);
-      if (ok) ok = wait_ab(bfull, 0, &s_abort);
-      if (ok) {
+      // (a half-range item leaves its rows unnormalised to the merge kernel)
+      if (ok && full) ok = wait_ab(pfull(n % kNBuf), (n / kNBuf) & 1, &s_abort);
+      if (ok && full) ok = wait_ab(bfull, 0, &s_abort);
+      if (ok && full) {
         ptx::tc_fence_after();
         const uint32_t kb = ptx::smem_u32(k_s);
         const uint64_t dbb = VH == 64 ? ptx::smem_desc_mn128(kb, kBBytes) : ptx::smem_desc_mn64(kb, kBBytes);
@@ -365,7 +387,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       ptx::tmem_ld_wait();
 #pragma unroll
       for (int c = 0; c < NC; ++c) ptx::reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
-      const int64_t tile0 = (int64_t)j * kT;
+      const int64_t tile0 = (int64_t)(tb + j) * kT;
       if (tile0 + kT > causal_from) {  // only the tiles that reach the chunk
         const int64_t rel = lim - tile0;  // keys i >= rel of this tile are masked for this row
 #pragma unroll
@@ -433,7 +455,26 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
     }
     // ---- epilogue: A operand of the B GEMM = OL restricted to the row's agent
     if (ok) ok = wait_pv(n - 1);  // every P.V MMA has finished
-    if (ok) {
+    if (ok && !full) {
+      // half-range item: this row's O and OL against m_used, then m_used and l
+      ptx::tc_fence_after();
+      float *rec = p.part + ((((int64_t)(pr - p.n_full) * 2 + part_half) * 2 + rank) * kM + row) *
+                                PartRec<D>::kFloats;
+#pragma unroll
+      for (int c = 0; c < (D + 64) / 32; ++c) {
+        uint32_t ov[32];
+        ptx::tmem_ld32(tmem + lane_base + kColO + c * 32, ov);
+        ptx::tmem_ld_wait();
+        ptx::reg_fence32(ov);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<float4 *>(rec + c * 32 + 4 * i) =
+              make_float4(__uint_as_float(ov[4 * i]), __uint_as_float(ov[4 * i + 1]), __uint_as_float(ov[4 * i + 2]),
+                          __uint_as_float(ov[4 * i + 3]));
+      }
+      *reinterpret_cast<float4 *>(rec + D + 64) = make_float4(m_used, l, 0.f, 0.f);
+    }
+    if (ok && full) {
       ptx::tc_fence_after();
       uint32_t olr[64];
       ptx::tmem_ld32(tmem + lane_base + kColOL, *reinterpret_cast<uint32_t(*)[32]>(&olr[0]));
@@ -469,7 +510,7 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
       if (lane == 0) ptx::mbar_arrive_cluster_relaxed(lead(pfull(n % kNBuf)));
       ok = wait_pv(n);  // the B GEMM, committed as "tile n"
     }
-    if (ok) {
+    if (ok && full) {
       ptx::tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       float *orow = a >= 0 ? p.O + (((int64_t)a * p.chunk + pos) * p.hq + head * p.G + g) * D : nullptr;
@@ -503,6 +544,46 @@ prefill_pair_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
   }
 }
 
+// Merge of a split pair's two half-range items (LRAgent technical summary,
+// Metodologia section 3: O = (P.V_base + (P.L_a).B_a) / l over all keys).
+// Per query row the two records are combined as online softmax combines two
+// blocks (each scaled by 2^(m_half - m), m the larger running max), OL is
+// restricted to the row's agent and multiplied by B_a in fp32, and O is
+// written.  One warp per row; lanes over the output columns.
+template <int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const Params p, const __nv_bfloat16 *__restrict__ B) {
+  constexpr int RF = PartRec<D>::kFloats;
+  __shared__ float s_ol[8][64];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t gw = (int64_t)blockIdx.x * 8 + warp;  // [split pair][CTA rank][row]
+  if (gw >= (int64_t)p.n_split * 2 * kM) return;
+  const int sp = (int)(gw / (2 * kM)), rank = (int)((gw / kM) & 1), row = (int)(gw % kM);
+  const int pr = p.n_full + sp;
+  const int head = pr % p.hkv, qbp = p.n_qbp - 1 - pr / p.hkv;
+  if (row >= p.rows) return;
+  const int a = row / p.rpa, pos = (2 * qbp + rank) * p.QB + (row / p.G) % p.QB, g = row % p.G;
+  if (pos >= p.chunk) return;
+  const float *r0 = p.part + ((((int64_t)sp * 2 + 0) * 2 + rank) * kM + row) * RF;
+  const float *r1 = p.part + ((((int64_t)sp * 2 + 1) * 2 + rank) * kM + row) * RF;
+  const float m0 = r0[D + 64], l0 = r0[D + 65], m1 = r1[D + 64], l1 = r1[D + 65];
+  const float m = fmaxf(m0, m1);
+  const float w0 = m0 == -INFINITY ? 0.f : exp2f(m0 - m);
+  const float w1 = m1 == -INFINITY ? 0.f : exp2f(m1 - m);
+  const float lt = w0 * l0 + w1 * l1;
+  const float inv = lt > 0.f ? 1.f / lt : 0.f;
+  for (int c = lane; c < 64; c += 32) s_ol[warp][c] = (w0 * r0[D + c] + w1 * r1[D + c]) * inv;
+  __syncwarp();
+  const int base_k = a * p.r, base_c = a * p.l_agent_stride;
+  const int64_t ldb = (int64_t)p.hkv * D;
+  const __nv_bfloat16 *bh = B + (int64_t)base_k * ldb + head * D;
+  float *orow = p.O + (((int64_t)a * p.chunk + pos) * p.hq + head * p.G + g) * D;
+  for (int d = lane; d < D; d += 32) {
+    float o = (w0 * r0[d] + w1 * r1[d]) * inv;
+    for (int k = 0; k < p.r; ++k) o = fmaf(s_ol[warp][base_c + k], __bfloat162float(bh[(int64_t)k * ldb + d]), o);
+    orow[d] = o;
+  }
+}
+
 }  // namespace ptp
 
 // ---------------------------------------------------------------------------
@@ -516,11 +597,13 @@ inline const char *prefill_tcgen05_last_error() { return prefill_tcgen05_err(); 
 
 struct PrefillTcgen05Plan {
   int D, QB, rows, l_width, T, nk, nv, smem_bytes, n_qbp;
+  int n_full, n_split;   // work items: whole-range pairs, pairs split over two items
+  size_t part_bytes;     // workspace the split pairs' row records need
   bool ok;
 };
 
 // Shape limits, query block, tile and ring depths of the tcgen05 prefill.
-inline PrefillTcgen05Plan prefill_tcgen05_plan(const fla_attn_dims &d, int chunk) {
+inline PrefillTcgen05Plan prefill_tcgen05_plan(const fla_attn_dims &d, int chunk, int64_t n0) {
   PrefillTcgen05Plan pl{};
   pl.ok = false;
   if (d.dtype != FLA_BF16) return pl;
@@ -549,14 +632,35 @@ inline PrefillTcgen05Plan prefill_tcgen05_plan(const fla_attn_dims &d, int chunk
   pl.smem_bytes = q_bytes + pl.nk * k_bytes + pl.nv * vl_bytes + 1024;
   const int n_qb = (chunk + QB - 1) / QB;
   pl.n_qbp = (n_qb + 1) / 2;
+  // The pairs of a last, partly filled wave run as two half-range items each
+  // (merged afterwards), so that wave ends about halfway; with fewer pairs
+  // than half the pair slots, every pair is split.  Only pairs of at least two
+  // key tiles split; the last pairs of the launch order have the fewest keys.
+  const int64_t pairs = (int64_t)d.hkv * pl.n_qbp;
+  const int slots = device_sm_count() / 2;
+  const int64_t min_tiles = (n0 + std::min(chunk, 2 * QB) + pl.T - 1) / pl.T;
+  int64_t n_split = 0;
+  if (min_tiles >= 2 && slots > 0) {
+    if (2 * pairs <= slots) n_split = pairs;
+    else if (pairs % slots != 0 && 2 * (pairs % slots) <= slots) n_split = pairs % slots;
+  }
+  pl.n_split = (int)n_split;
+  pl.n_full = (int)(pairs - n_split);
+  pl.part_bytes = (size_t)n_split * 2 * 2 * ptp::kM * (D == 128 ? ptp::PartRec<128>::kFloats : ptp::PartRec<64>::kFloats) * 4;
   pl.ok = true;
   return pl;
 }
 
 inline fla_status prefill_tcgen05_launch(const fla_attn_dims &d, float scale, const void *Q, const void *K,
                                          const void *V, const void *L, const void *B, int64_t n0, int chunk, float *O,
-                                         cudaStream_t s) {
-  const PrefillTcgen05Plan pl = prefill_tcgen05_plan(d, chunk);
+                                         void *workspace, size_t workspace_bytes, cudaStream_t s) {
+  PrefillTcgen05Plan pl = prefill_tcgen05_plan(d, chunk, n0);
+  if (pl.ok && pl.n_split > 0 &&
+      (workspace == nullptr || workspace_bytes < pl.part_bytes || (reinterpret_cast<uintptr_t>(workspace) & 15u))) {
+    // no room for the split pairs' records: every pair runs its whole range
+    pl.n_full += pl.n_split;
+    pl.n_split = 0;
+  }
   if (!pl.ok) {
     prefill_tcgen05_err() = "shape outside the tcgen05 prefill kernel";
     return FLA_ERR_UNSUPPORTED;
@@ -619,7 +723,11 @@ inline fla_status prefill_tcgen05_launch(const fla_attn_dims &d, float scale, co
   prm.l_agent_stride = (int)d.l_agent_stride;
   prm.nk = pl.nk; prm.nv = pl.nv;
   prm.scale_log2 = scale * 1.4426950408889634f;
-  const int64_t grid64 = 2LL * d.hkv * pl.n_qbp;
+  prm.n_qbp = pl.n_qbp;
+  prm.n_full = pl.n_full;
+  prm.n_split = pl.n_split;
+  prm.part = reinterpret_cast<float *>(workspace);
+  const int64_t grid64 = 2LL * (pl.n_full + 2LL * pl.n_split);
   if (grid64 > 0x7fffffffLL || n_total > 0x7fffffffLL) {
     prefill_tcgen05_err() = "chunk or context too large";
     return FLA_ERR_UNSUPPORTED;
@@ -637,16 +745,21 @@ inline fla_status prefill_tcgen05_launch(const fla_attn_dims &d, float scale, co
   cfg.attrs = at;
   cfg.numAttrs = 1;
   cudaError_t e = cudaSuccess;
-#define FLA_PTP_CASE(DD)                                                                 \
-  if (D == DD) {                                                                         \
-    auto kern = ptp::prefill_pair_kernel<DD>;                                            \
-    e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), pl.smem_bytes);       \
-    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, mK, mV, mL, mB, prm);      \
-    if (e != cudaSuccess) {                                                              \
-      prefill_tcgen05_err() = cudaGetErrorString(e);                                     \
-      return FLA_ERR_CUDA;                                                               \
-    }                                                                                    \
-    return FLA_OK;                                                                       \
+  const unsigned merge_blocks = (unsigned)((2LL * ptp::kM * pl.n_split + 7) / 8);  // one warp per row
+#define FLA_PTP_CASE(DD)                                                                                \
+  if (D == DD) {                                                                                        \
+    auto kern = ptp::prefill_pair_kernel<DD>;                                                           \
+    e = ensure_dynamic_smem(reinterpret_cast<const void *>(kern), pl.smem_bytes);                      \
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, kern, mK, mV, mL, mB, prm);                     \
+    if (e == cudaSuccess && pl.n_split > 0) {                                                           \
+      ptp::prefill_merge_kernel<DD><<<merge_blocks, 256, 0, s>>>(prm, reinterpret_cast<const __nv_bfloat16 *>(B)); \
+      e = cudaGetLastError();                                                                           \
+    }                                                                                                   \
+    if (e != cudaSuccess) {                                                                             \
+      prefill_tcgen05_err() = cudaGetErrorString(e);                                                    \
+      return FLA_ERR_CUDA;                                                                              \
+    }                                                                                                   \
+    return FLA_OK;                                                                                      \
   }
   FLA_PTP_CASE(128) FLA_PTP_CASE(64)
 #undef FLA_PTP_CASE

@@ -214,8 +214,13 @@ FLA_API fla_status flash_lora_attn_decode(const fla_attn_dims *dims, const void 
  *                                                 by lr_cache_build beforehand)
  *   B        [A, r, hkv*d]                       (input)
  *   O        fp32 [A, chunk, hq, d]              (output)
- *   workspace as for decode, flash_lora_attn_prefill_workspace_size() bytes
- *            (may be 0 bytes / NULL when the size query returns 0).
+ *   workspace flash_lora_attn_prefill_workspace_size() bytes, 16-byte aligned
+ *            (may be 0 bytes / NULL when the size query returns 0).  The
+ *            tcgen05 kernel uses it to run the CTA pairs of a last, partly
+ *            filled wave as two half-range items whose row records a merge
+ *            kernel combines; with a smaller or unaligned workspace it runs
+ *            every pair over its whole key range instead (same results up to
+ *            rounding, no error).  Calls on one stream may share it.
  * Kernels: tcgen05 (bf16; head_dim 64 or 128; A*(hq/hkv) <= 128; L width
  * (r, or A*r) <= 64 and A*r <= 64; l_agent_stride 0 or r); mma.sync (bf16;
  * head_dim 64 or 128; r % 16 == 0, r <= 64; l_agent_stride 0 or r); both need

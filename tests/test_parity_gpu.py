@@ -288,6 +288,27 @@ def test_prefill_tcgen05_shapes(case, kernel):
     check_attn(O, ref, what=f"prefill {kernel} {case}")
 
 
+@pytest.mark.parametrize("case", [(4, 32, 8, 128, 16, 1000, 200), (2, 8, 8, 64, 32, 700, 90)], ids=["d128", "d64"])
+def test_prefill_tcgen05_split_tail_and_whole_range_both_match(case):
+    """With its workspace the tcgen05 prefill runs pairs as two half-range items merged afterwards (every
+    pair here: few pairs); with no workspace every pair runs its whole key range.  Both against the oracle."""
+    A, hq, hkv, d, r, n0, c = case
+    w = small_prefill(A, hq, hkv, d, r, n0, c)
+    x = make_prefill_inputs(w, seed=7, with_X=False)
+    dx = to_dev(x)
+    ref = oracle.prefill(x["Q"], x["K_base"], x["V_base"], x["L"], x["B"], n0=n0, rank=r)
+    fla = _fla()
+    need = fla.load_library().flash_lora_attn_prefill_workspace_size(
+        __import__("ctypes").byref(fla.binding.make_dims(A, hq, hkv, d, r, 1, A * r, r, None, "tcgen05")), c, n0)
+    assert need > 0  # this shape splits
+    O_split = fla.flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], n0, rank=r,
+                                          kernel="tcgen05")
+    O_whole = fla.flash_lora_attn_prefill(dx["Q"], dx["K_base"], dx["V_base"], dx["L"], dx["B"], n0, rank=r,
+                                          kernel="tcgen05", workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))
+    check_attn(O_split, ref, what=f"prefill split {case}")
+    check_attn(O_whole, ref, what=f"prefill whole {case}")
+
+
 def test_prefill_tcgen05_rejects_shapes_outside_it():
     w = small_prefill(3, 16, 4, 128, 32, 1, 20)  # L width A*r = 96 > 64
     dx = to_dev(make_prefill_inputs(w, seed=1, with_X=False))
