@@ -427,7 +427,8 @@ def _median_launch_s(fn, reps, stream, flush=None, settle=False):
     kernels the call enqueues (no host-side argument handling); an optional
     L2 flush runs between replays, outside the events.  settle: start after
     one idle second, so that a tensor-bound leg is not measured under the power
-    cap its predecessors in the same process pushed the GPU into.
+    cap its predecessors in the same process pushed the GPU into; the timed
+    replays then follow 0.25 s of untimed ones, which bring the clocks back up.
     """
     import torch
 
@@ -441,6 +442,12 @@ def _median_launch_s(fn, reps, stream, flush=None, settle=False):
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         fn()
+    if settle:
+        t_end = time.perf_counter() + 0.25
+        with torch.cuda.stream(stream):
+            while time.perf_counter() < t_end:
+                graph.replay()
+                stream.synchronize()
     times = []
     with torch.cuda.stream(stream):
         graph.replay()
