@@ -428,7 +428,9 @@ def _median_launch_s(fn, reps, stream, flush=None, settle=False):
     L2 flush runs between replays, outside the events.  settle: start after
     one idle second, so that a tensor-bound leg is not measured under the power
     cap its predecessors in the same process pushed the GPU into; the timed
-    replays then follow 0.25 s of untimed ones, which bring the clocks back up.
+    replays then follow 20 ms of untimed ones, which bring the clocks back up
+    from idle without heating the GPU into the power cap (the legs are burst
+    measurements, against the burst peak).
     """
     import torch
 
@@ -443,7 +445,7 @@ def _median_launch_s(fn, reps, stream, flush=None, settle=False):
     with torch.cuda.graph(graph, stream=stream):
         fn()
     if settle:
-        t_end = time.perf_counter() + 0.25
+        t_end = time.perf_counter() + 0.02
         with torch.cuda.stream(stream):
             while time.perf_counter() < t_end:
                 graph.replay()
